@@ -1,0 +1,8 @@
+"""Float64 CPU oracle for exact attention forward (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The product path never does.
+"""
+from .attention import (attention, attention_bruteforce, attention_head,  # noqa: F401
+                        attention_online_head, causal_visible, kv_head_of, lse_merge,
+                        probs_head, scores_head)
