@@ -1,0 +1,370 @@
+"""Attention-forward benchmark: device-timed TFLOPS on GB300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+
+A step is one attention forward (the whole path: every kernel attn_fwd
+launches) over one batch of the workload's seeded synthetic inputs, already
+resident in HBM.  Between timed steps a 512 MiB buffer is rewritten to flush
+L2, outside the per-step CUDA events.  FLOPs = 4*B*Hq*Nq*Nkv*D, halved when
+causal.  Under torchrun every rank runs the full workload on its own GPU
+(weak scaling, no data-path collective); the reported time is the max over
+ranks and the value is the FLOPs of all ranks over that time.
+
+``--impl reference`` times the float64 CPU oracle on the host cores instead
+(there is no other implementation of this path to run), on a bounded sample
+of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from exact_attention_attn_gb300.workloads import BENCH_WORKLOAD, WORKLOADS, make_workload_inputs, to_f64  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def reduce_max(x: float, ws: int, device=None) -> float:
+    """Max of a host scalar over ranks (timing only, not the data path)."""
+    if ws <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device_index = device_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, row[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# ncu traffic recorded in profiles/ (null when the kernel source changed since)
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_attn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """Parse profiles/ncu_traffic.md rows: | workload | kernel | source hash | bytes per launch |"""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None, None
+    cur = kernel_source_hash()
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == workload and cells[2] == cur:
+            try:
+                return float(cells[3]), cells[1]
+            except ValueError:
+                pass
+    return None, None
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else None
+    except Exception:
+        return None
+
+
+def time_oracle(w, q, k, v, budget_s: float, max_heads: int | None = None):
+    """Run the oracle head by head over the workload until budget_s seconds
+    have passed (at least one head).  Returns (TFLOPS, heads, seconds)."""
+    import oracle
+    B, Hq = w.B, w.Hq
+    heads = [(b, h) for b in range(B) for h in range(Hq)]
+    if max_heads:
+        heads = heads[:max_heads]
+    per_head_flops = w.flops() / (B * Hq)
+    done = 0
+    t0 = time.perf_counter()
+    group = w.Hq // w.Hkv
+    for b, h in heads:
+        qh = to_f64(q[b, h])
+        kh = to_f64(k[b, h // group])
+        vh = to_f64(v[b, h // group])
+        oracle.attention_head(qh, kh, vh, w.scale, w.causal)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return per_head_flops * done / dt / 1e12, done, dt
+
+
+# --------------------------------------------------------------------------
+
+def run_reference(args, w):
+    ws, rank, _ = dist_info()
+    if ws > 1 and rank != 0:
+        return 0
+    q, k, v = make_workload_inputs(w)
+    per_step_budget = 5.0
+    for _ in range(args.warmup):
+        time_oracle(w, q, k, v, budget_s=0.0, max_heads=1)
+    vals, heads_total, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        tf, heads, dt = time_oracle(w, q, k, v, budget_s=per_step_budget)
+        vals.append(tf)
+        heads_total += heads
+        secs += dt
+    value = statistics.mean(vals)
+    cores = blas_threads() or cpu_cores()
+    sample = (f"{heads_total} (b,hq) heads of {w.name} in total over {args.steps} steps, all {w.Nq} query rows each, "
+              f"float64 numpy on the host; each step stops after {per_step_budget:.0f} s")
+    flops_per_head = w.flops() / (w.B * w.Hq)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 0 if ws <= 1 else ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(w.describe(), l2="n/a (host)"),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "flops_per_head": flops_per_head,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "attn fwd TFLOPS (bf16, device-timed, 1 GPU) and % of GB300 dense BF16 peak"
+
+
+def run_ours(args, w):
+    from exact_attention_attn_gb300 import attn_fwd, attn_fwd_host, attn_fwd_status, load_library
+
+    ws, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    load_library()
+    peaks, peak_src = load_peaks()
+
+    q, k, v = make_workload_inputs(w)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty((w.B, w.Hq, w.Nq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream)
+    torch.cuda.synchronize(dev)
+    st = attn_fwd_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    time.sleep(0.25)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)                      # L2 flush, outside the events
+        starts[i].record(stream)
+        attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    st = attn_fwd_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = statistics.mean(step_ms)
+    ms = reduce_max(ms_local, ws, dev)
+    flops = w.flops()
+    value = flops * max(ws, 1) / (ms * 1e-3) / 1e12
+
+    # roofline of the dominant (here: the only) kernel of a step
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    traffic, traffic_kernel = recorded_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_source": f"{peak_src} bf16 dense burst",
+                "algorithmic_flops_per_launch": flops, "algorithmic_hbm_bytes_per_launch": w.hbm_bytes(),
+                "achieved_hbm_gbs": w.hbm_bytes() / (ms_local * 1e-3) / 1e9,
+                "kernel": traffic_kernel}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pq, pk, pv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        po = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        pl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        for _ in range(2):
+            attn_fwd_host(pq, pk, pv, scale=w.scale, causal=w.causal, device=dev, out=po, lse=pl)
+        n_e2e = max(3, min(args.steps, 20))
+        barrier(ws)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            attn_fwd_host(pq, pk, pv, scale=w.scale, causal=w.causal, device=dev, out=po, lse=pl)
+        dt = (time.perf_counter() - t0) / n_e2e
+        dt = reduce_max(dt, ws, dev)
+        e2e = {"value": flops * max(ws, 1) / dt / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": int(q.numel() * 2 + k.numel() * 2 + v.numel() * 2),
+               "d2h_bytes_per_step": int(out.numel() * 2 + lse.numel() * 4), "ms_per_step": dt * 1e3,
+               "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and ws <= 1 and not args.no_cpu_baseline:
+        tf, heads, dt = time_oracle(w, q, k, v, budget_s=args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": blas_threads() or cpu_cores(), "kind": "oracle",
+               "sample": f"{heads} of {w.B * w.Hq} (b,hq) heads of {w.name}, all {w.Nq} rows each, "
+                         f"float64 numpy, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": max(ws, 1), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(w.describe(), l2="flushed between steps (512 MiB write, outside the events)",
+                           parallelism=f"replicas x{max(ws, 1)}" if ws > 1 else "1 GPU"),
+            "pct_of_peak": 100.0 * value / max(ws, 1) / peak,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * kernels_per_call(w),
+            "clocks": clocks, "timed_wall_s": t_wall,
+            "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)},
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def kernels_per_call(w) -> int:
+    from exact_attention_attn_gb300.binding import attn_fwd_plan
+    return attn_fwd_plan(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal)["launches"]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,172 @@
+"""ctypes binding of the C ABI in include/attn.h (argument marshalling only).
+
+Every step of the attention forward runs in the CUDA kernels of
+libattn_gb300.so.  torch provides device memory and the current stream; there
+is no CPU or library fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libattn_gb300.so"
+_lib = None
+_lock = threading.Lock()
+
+ATTN_OK = 0
+_ERRORS = {-1: "ATTN_ERR_ARG", -2: "ATTN_ERR_ALIGN", -3: "ATTN_ERR_ARCH", -4: "ATTN_ERR_LAUNCH",
+           -5: "ATTN_ERR_TIMEOUT", -6: "ATTN_ERR_NOMEM", -7: "ATTN_ERR_DEVICE"}
+
+
+class AttnPlan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("launches", ctypes.c_int), ("grid", ctypes.c_int),
+                ("kv_splits", ctypes.c_int), ("d_slices", ctypes.c_int), ("workspace_bytes", ctypes.c_longlong)]
+
+
+PATH_NAMES = {0: "none", 1: "simt", 2: "tc", 3: "tc_splitkv"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {_ERRORS.get(code, code)}: {attn_strerror(code)}"
+                         + (f" ({_last_cuda_error()})" if code == -4 else ""))
+
+
+def library_path() -> str:
+    return os.environ.get("ATTN_GB300_LIB", os.path.join(_PKG, _LIB_NAME))
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libattn_gb300.so once; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it first with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'` "
+                              "(there is no fallback implementation)")
+        lib = ctypes.CDLL(path)
+        vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+        lib.attn_fwd.restype = ci
+        lib.attn_fwd_status.argtypes = [vp]
+        lib.attn_fwd_status.restype = ci
+        lib.attn_strerror.argtypes = [ci]
+        lib.attn_strerror.restype = ctypes.c_char_p
+        lib.attn_last_cuda_error.argtypes = []
+        lib.attn_last_cuda_error.restype = ctypes.c_char_p
+        lib.attn_fwd_plan.argtypes = [ci, ci, ci, ci, ci, ci, ci, ctypes.POINTER(AttnPlan)]
+        lib.attn_fwd_plan.restype = ci
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = ci
+        _lib = lib
+        return lib
+
+
+def attn_strerror(code: int) -> str:
+    return load_library().attn_strerror(int(code)).decode()
+
+
+def _last_cuda_error() -> str:
+    return load_library().attn_last_cuda_error().decode()
+
+
+def attn_version() -> int:
+    return int(load_library().attn_version())
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, ndim: int):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+             causal: bool = False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+             stream=None):
+    """O, LSE = attention forward of bf16 q [B,Hq,Nq,D], k and v [B,Hkv,Nkv,D].
+
+    O is bf16 [B,Hq,Nq,D]; LSE is fp32 [B,Hq,Nq] (natural log).  Runs
+    asynchronously on ``stream`` (default: torch's current stream).
+    """
+    lib = load_library()
+    _check(q, "q", torch.bfloat16, 4)
+    _check(k, "k", torch.bfloat16, 4)
+    _check(v, "v", torch.bfloat16, 4)
+    B, Hq, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError(f"k {tuple(k.shape)} / v {tuple(v.shape)} do not match q {tuple(q.shape)}")
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, Nq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    _check(out, "out", torch.bfloat16, 4)
+    _check(lse, "lse", torch.float32, 3)
+    if tuple(out.shape) != (B, Hq, Nq, D) or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("out / lse shape mismatch")
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          B, Hq, Hkv, Nq, Nkv, D, float(scale), int(bool(causal)), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+                  causal: bool = False, device=None, out: torch.Tensor | None = None,
+                  lse: torch.Tensor | None = None):
+    """Host-buffer form of attn_fwd: copies q, k, v (CPU, ideally pinned) to
+    the device, runs the kernel, copies O and LSE back into host tensors and
+    waits for them.  Returns (O, LSE) on the CPU."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    dq = q.to(dev, non_blocking=True)
+    dk = k.to(dev, non_blocking=True)
+    dv = v.to(dev, non_blocking=True)
+    do, dl = attn_fwd(dq, dk, dv, scale=scale, causal=causal, stream=stream)
+    if out is None:
+        out = torch.empty(do.shape, dtype=do.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty(dl.shape, dtype=dl.dtype, pin_memory=True)
+    out.copy_(do, non_blocking=True)
+    lse.copy_(dl, non_blocking=True)
+    stream.synchronize()
+    return out, lse
+
+
+def attn_fwd_plan(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int, causal: bool) -> dict:
+    """The kernels attn_fwd would launch for these sizes on the current device."""
+    plan = AttnPlan()
+    rc = load_library().attn_fwd_plan(B, Hq, Hkv, Nq, Nkv, D, int(bool(causal)), ctypes.byref(plan))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_plan")
+    d = {f: getattr(plan, f) for f, _ in AttnPlan._fields_}
+    d["path_name"] = PATH_NAMES.get(plan.path, str(plan.path))
+    return d
+
+
+def attn_fwd_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(load_library().attn_fwd_status(_stream_handle(stream)))

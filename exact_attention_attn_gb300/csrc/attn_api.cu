@@ -1,0 +1,181 @@
+// Host side of the C ABI declared in include/attn.h: argument checks, the
+// per-device status word, and the choice of kernel.
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+// Device status word: the first kernel error on a device wins; attn_fwd_status
+// reads and clears it.
+__device__ int g_status;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  bool arch_ok = false;
+  int sm_count = 0;
+  int *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+thread_local char t_last_error[256] = "";
+
+int record(cudaError_t e) {
+  snprintf(t_last_error, sizeof(t_last_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return ATTN_ERR_LAUNCH;
+}
+
+// Reads the compute capability and the status word's device address once
+// per device (with that device current).
+int device_info(DeviceInfo **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_ARCH;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return record(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return record(e);
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return record(e);
+    d.arch_ok = (major == 10 && minor == 3);
+    d.sm_count = sms;
+    if (d.arch_ok) {
+      void *ptr = nullptr;
+      if ((e = cudaGetSymbolAddress(&ptr, g_status)) != cudaSuccess) return record(e);
+      d.status = static_cast<int *>(ptr);
+    }
+    d.ready = true;
+  }
+  if (!d.arch_ok) return ATTN_ERR_ARCH;
+  *out = &d;
+  return ATTN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal) {
+  if (B < 0 || Nq < 0 || Nkv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_ARG;
+  if (D < 64 || D > ATTN_MAX_HEAD_DIM || D % 64 != 0) return ATTN_ERR_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
+  // element counts must fit the kernels' 64-bit index math with room to spare
+  if ((int64_t)B * Hq * Nq * (int64_t)D > (int64_t)1 << 46) return ATTN_ERR_ARG;
+  if ((int64_t)B * Hkv * Nkv * (int64_t)D > (int64_t)1 << 46) return ATTN_ERR_ARG;
+  return ATTN_OK;
+}
+
+void make_plan(const Problem &p, const DeviceInfo &dev, attn_plan *plan) {
+  (void)dev;
+  memset(plan, 0, sizeof(*plan));
+  if (p.B == 0 || p.Nq == 0) {
+    plan->path = ATTN_PATH_NONE;
+    plan->kv_splits = 1;
+    plan->d_slices = 1;
+    return;
+  }
+  plan->path = ATTN_PATH_SIMT;
+  plan->launches = 1;
+  plan->kv_splits = 1;
+  plan->d_slices = (p.D + 255) / 256;
+  plan->grid = (int)(((int64_t)(p.Nq + 63) / 64) * p.B * p.Hq * plan->d_slices);
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_version(void) { return 100; /* 0.1.0 */ }
+
+const char *attn_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_ARG: return "invalid argument (null pointer, bad size, Hq % Hkv != 0, unsupported D or non-finite scale)";
+    case ATTN_ERR_ALIGN: return "tensor base address not 16-byte aligned";
+    case ATTN_ERR_ARCH: return "current device is not an sm_103 (compute capability 10.3) GPU";
+    case ATTN_ERR_LAUNCH: return "CUDA error (see attn_last_cuda_error)";
+    case ATTN_ERR_TIMEOUT: return "a bounded device-side wait ran out; outputs undefined";
+    case ATTN_ERR_NOMEM: return "could not allocate the split-KV workspace";
+    case ATTN_ERR_DEVICE: return "a kernel consistency check failed; outputs undefined";
+    default: return "unknown attn error code";
+  }
+}
+
+const char *attn_last_cuda_error(void) { return attn::t_last_error; }
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+             float scale, int causal, attn_stream_t stream) {
+  using namespace attn;
+  int rc = check_sizes(B, Hq, Hkv, Nq, Nkv, D, causal);
+  if (rc != ATTN_OK) return rc;
+  if (!isfinite(scale)) return ATTN_ERR_ARG;
+  if (B == 0 || Nq == 0) return ATTN_OK;
+  if (!q || !o || !lse) return ATTN_ERR_ARG;
+  if (Nkv > 0 && (!k || !v)) return ATTN_ERR_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
+  if (Nkv > 0 && (!aligned16(k) || !aligned16(v))) return ATTN_ERR_ALIGN;
+
+  DeviceInfo *dev = nullptr;
+  rc = device_info(&dev);
+  if (rc != ATTN_OK) return rc;
+
+  Problem p;
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.k = static_cast<const __nv_bfloat16 *>(k);
+  p.v = static_cast<const __nv_bfloat16 *>(v);
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.lse = lse;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.Nkv = Nkv; p.D = D;
+  p.scale = scale;
+  p.causal = causal;
+  p.status = dev->status;
+
+  attn_plan plan;
+  make_plan(p, *dev, &plan);
+  cudaError_t e = launch_simt(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record(e);
+  return ATTN_OK;
+}
+
+int attn_fwd_plan(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, attn_plan *plan) {
+  using namespace attn;
+  if (!plan) return ATTN_ERR_ARG;
+  int rc = check_sizes(B, Hq, Hkv, Nq, Nkv, D, causal);
+  if (rc != ATTN_OK) return rc;
+  DeviceInfo *dev = nullptr;
+  rc = device_info(&dev);
+  if (rc != ATTN_OK) return rc;
+  Problem p{};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.Nkv = Nkv; p.D = D; p.causal = causal;
+  make_plan(p, *dev, plan);
+  return ATTN_OK;
+}
+
+int attn_fwd_status(attn_stream_t stream) {
+  using namespace attn;
+  DeviceInfo *dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != ATTN_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record(e);
+  int h = 0;
+  if ((e = cudaMemcpy(&h, dev->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return record(e);
+  if (h != 0) {
+    const int zero = 0;
+    if ((e = cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) return record(e);
+  }
+  return h;
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// Internal declarations shared by the host launcher and the kernel
+// translation units of libattn_gb300.so.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace attn {
+
+// One attention forward problem, as validated by attn_fwd.
+struct Problem {
+  const __nv_bfloat16 *q;  // [B, Hq, Nq, D]
+  const __nv_bfloat16 *k;  // [B, Hkv, Nkv, D]
+  const __nv_bfloat16 *v;  // [B, Hkv, Nkv, D]
+  __nv_bfloat16 *o;        // [B, Hq, Nq, D]
+  float *lse;              // [B, Hq, Nq]
+  int B, Hq, Hkv, Nq, Nkv, D;
+  float scale;
+  int causal;
+  int *status;             // device status word (first error wins)
+};
+
+// Device status codes written by kernels (same values as the public ATTN_ERR_*).
+constexpr int kStatusTimeout = -5;
+constexpr int kStatusDevice = -7;
+
+// Plain CUDA-core kernel: correct for every supported shape; used for the
+// shapes the tensor-core kernel does not take.
+cudaError_t launch_simt(const Problem &p, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,140 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact attention forward library
+ * (libattn_gb300.so).
+ *
+ * The operation.  For every batch b and query head hq, with key/value head
+ * kv = hq / (Hq / Hkv):
+ *
+ *     S   = scale * Q[b,hq] K[b,kv]^T                      (Nq x Nkv)
+ *     S_ij = -inf where causal and j > i + (Nkv - Nq)
+ *     O   = softmax_rows(S) V[b,kv]                        (Nq x D)
+ *     LSE_i = ln sum_j exp(S_ij)
+ *
+ * Sources (page title, section):
+ *   - "FlashAttention: Fast and Memory-Efficient Exact Attention with
+ *     IO-Awareness" (summary card): exact attention computed in SRAM-sized
+ *     tiles; the N x N score matrix is never written to HBM.
+ *   - "FlashAttention v1/v2/v3/v4: el bibliotecario que nunca despeja la mesa"
+ *     (lo0.es), "El truco que hizo posible todo: online softmax": the running
+ *     max m and running sum l; the result equals the standard softmax.
+ *   - "ffpa-attn 0.2.3" (FFPA README), feature table and "Quick Start":
+ *     (B, H, N, D) layout, self-attention, cross-attention (Nq != Nkv),
+ *     GQA/MQA (Hq != Hkv), causal masking, head dims up to 1024;
+ *     "Split-D and TiledMMA": the D axis is split so on-chip staging does not
+ *     grow with D.
+ *   - "ZYFA: FP8 FlashAttention Kernels for AMD MI355X", "The details that
+ *     make it production-grade" and "Getting started with ZYFA": LSE for
+ *     merging partial results over key ranges; a call that never waits on
+ *     the host.
+ *
+ * Conventions the pages leave open (chosen here): LSE is the natural log;
+ * causal masking with Nq != Nkv is bottom-right aligned; a query row that
+ * sees no key gets O = 0 and LSE = -inf; GQA groups are consecutive query
+ * heads.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *attn_stream_t;
+
+/* Return codes.  0 is success; every error is negative. */
+#define ATTN_OK 0
+#define ATTN_ERR_ARG (-1)     /* a null pointer, a bad size, Hq % Hkv != 0, an unsupported D, a non-finite scale */
+#define ATTN_ERR_ALIGN (-2)   /* a tensor base address not 16-byte aligned */
+#define ATTN_ERR_ARCH (-3)    /* the current device is not a compute capability 10.3 GPU (sm_103) */
+#define ATTN_ERR_LAUNCH (-4)  /* a CUDA runtime or driver call failed; attn_last_cuda_error() has its text */
+#define ATTN_ERR_TIMEOUT (-5) /* a kernel's bounded wait ran out (reported by attn_fwd_status) */
+#define ATTN_ERR_NOMEM (-6)   /* the split-KV workspace could not be allocated */
+#define ATTN_ERR_DEVICE (-7)  /* a kernel's own consistency check failed (reported by attn_fwd_status) */
+
+#define ATTN_MAX_HEAD_DIM 1024
+
+/*
+ * attn_fwd -- exact scaled-dot-product attention forward, bf16 in, bf16 O and
+ * fp32 LSE out.
+ *
+ * q    device pointer, bf16, [B, Hq, Nq, D], contiguous (D fastest).
+ * k, v device pointers, bf16, [B, Hkv, Nkv, D], contiguous.
+ * o    device pointer, bf16, [B, Hq, Nq, D], contiguous; fully written.
+ * lse  device pointer, fp32, [B, Hq, Nq]; fully written (natural log).
+ * B, Nq, Nkv >= 0; Hq >= 1, Hkv >= 1, Hq % Hkv == 0.  B * Nq == 0 is an empty
+ *      problem (returns ATTN_OK without launching).  Nkv == 0 gives O = 0 and
+ *      LSE = -inf everywhere.
+ * D    head dim: a multiple of 64 in [64, 1024].
+ * scale  finite multiplier of Q K^T (1/sqrt(D) is the usual choice).
+ * causal  0 or 1; 1 masks key j for query i when j > i + (Nkv - Nq).
+ * stream  the CUDA stream to run on.
+ *
+ * All pointers are owned by the caller and must stay valid until the stream
+ * reaches the work.  o must not overlap q, k, v or lse.  Every base address
+ * must be 16-byte aligned.  The call validates its arguments on the host,
+ * launches asynchronously on `stream` and returns without waiting.  It may
+ * allocate a stream-ordered split-KV workspace (cudaMallocAsync on `stream`,
+ * freed on the same stream after use) when the problem has too few query
+ * tiles to fill the GPU.  Bounded device-side waits that run out are not
+ * reported here: call attn_fwd_status.
+ *
+ * Returns ATTN_OK or a negative ATTN_ERR_* code; on error nothing is launched.
+ */
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+             float scale, int causal, attn_stream_t stream);
+
+/*
+ * attn_fwd_status -- synchronise `stream`, then read and clear the device
+ * status word of the current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a
+ * bounded mbarrier wait inside a kernel gave up; that kernel's outputs are
+ * undefined), ATTN_ERR_DEVICE, or ATTN_ERR_LAUNCH if the synchronisation
+ * itself reported a CUDA error.
+ */
+ATTN_API int attn_fwd_status(attn_stream_t stream);
+
+/* Static description of a return code. */
+ATTN_API const char *attn_strerror(int code);
+
+/* Text of the last CUDA error seen by this library on the calling thread
+ * ("" if none). */
+ATTN_API const char *attn_last_cuda_error(void);
+
+/*
+ * attn_fwd_plan -- describe, without launching anything, the kernels attn_fwd
+ * would run for these sizes on the current device.  Sizes are checked as in
+ * attn_fwd (pointers are not involved).  Fills *plan and returns ATTN_OK, or
+ * returns a negative ATTN_ERR_* code.
+ */
+#define ATTN_PATH_NONE 0      /* empty problem: nothing is launched */
+#define ATTN_PATH_SIMT 1      /* CUDA-core kernel */
+#define ATTN_PATH_TC 2        /* tcgen05 tensor-core kernel */
+#define ATTN_PATH_TC_SPLITKV 3 /* tcgen05 kernel over key splits + LSE merge kernel */
+
+typedef struct attn_plan {
+  int path;                  /* ATTN_PATH_* */
+  int launches;              /* kernel launches per attn_fwd call */
+  int grid;                  /* CTAs of the main kernel */
+  int kv_splits;             /* key-range splits (1 = none) */
+  int d_slices;              /* output head-dim slices per query tile */
+  long long workspace_bytes; /* split-KV workspace allocated per call */
+} attn_plan;
+
+ATTN_API int attn_fwd_plan(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, attn_plan *plan);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

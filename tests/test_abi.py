@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/attn.h declares, and rejects bad arguments on the host before it
+touches a device."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_attn_gb300 import build as B
+    B.build()
+    from exact_attention_attn_gb300.binding import load_library
+    return load_library()
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            names.update(re.findall(r"ATTN_API\s+[\w\s\*]*?\b(attn_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"attn_fwd", "attn_fwd_status", "attn_strerror", "attn_version"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert names <= exported
+    # nothing else leaks out of the library's C ABI namespace
+    assert {n for n in exported if n.startswith("attn_")} == names
+
+
+def test_version_and_strerror(lib):
+    assert lib.attn_version() == 100
+    for code in range(0, -8, -1):
+        assert lib.attn_strerror(code)
+    assert b"unknown" in lib.attn_strerror(-99)
+
+
+class Buf:
+    """16-byte aligned host addresses; never dereferenced (argument checks
+    return before any device work)."""
+    def __init__(self):
+        self.raw = ctypes.create_string_buffer(256)
+        base = ctypes.addressof(self.raw)
+        self.p = (base + 15) & ~15
+
+
+def call(lib, q, k, v, o, l, B=1, Hq=2, Hkv=1, Nq=8, Nkv=8, D=64, scale=0.125, causal=0):
+    return lib.attn_fwd(q, k, v, o, l, B, Hq, Hkv, Nq, Nkv, D, scale, causal, None)
+
+
+def test_argument_errors(lib):
+    b = Buf()
+    p = b.p
+    ARG, ALIGN = -1, -2
+    assert call(lib, p, p, p, p, p, D=65) == ARG
+    assert call(lib, p, p, p, p, p, D=32) == ARG
+    assert call(lib, p, p, p, p, p, D=1088) == ARG
+    assert call(lib, p, p, p, p, p, Hq=3, Hkv=2) == ARG
+    assert call(lib, p, p, p, p, p, Hkv=0) == ARG
+    assert call(lib, p, p, p, p, p, B=-1) == ARG
+    assert call(lib, p, p, p, p, p, Nq=-5) == ARG
+    assert call(lib, p, p, p, p, p, scale=float("nan")) == ARG
+    assert call(lib, p, p, p, p, p, scale=float("inf")) == ARG
+    assert call(lib, p, p, p, p, p, causal=2) == ARG
+    assert call(lib, None, p, p, p, p) == ARG
+    assert call(lib, p, None, p, p, p) == ARG
+    assert call(lib, p, p, p, p, None) == ARG
+    assert call(lib, p + 2, p, p, p, p) == ALIGN
+    assert call(lib, p, p, p + 8, p, p) == ALIGN
+    assert call(lib, p, p, p, p, p + 4) == ALIGN
+    # empty problems succeed without touching a device
+    assert call(lib, None, None, None, None, None, B=0) == 0
+    assert call(lib, None, None, None, None, None, Nq=0) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    code = ("import exact_attention_attn_gb300 as A\n"
+            "try:\n    A.attn_version()\nexcept ImportError as e:\n    print('RAISED', e)\n")
+    env = dict(os.environ, ATTN_GB300_LIB=str(tmp_path / "nope.so"), PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+    assert "RAISED" in r.stdout and "no fallback" in r.stdout

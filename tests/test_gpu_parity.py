@@ -1,0 +1,105 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Tolerances (bf16 O, fp32 LSE): max|dO| <= 2e-2, mean|dO| <= 2e-3,
+max|dLSE| <= 1e-3.  The five named workloads run at their full sizes (rows
+sampled for the three large ones), plus a sweep over head dims, ragged
+lengths, GQA ratios, cross-attention and causal masking, and the edge cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_attn_gb300 import attn_fwd, attn_fwd_status
+from exact_attention_attn_gb300.workloads import WORKLOADS, WORKLOAD_ORDER, make_qkv, make_workload_inputs, \
+    sample_rows
+
+from parity_util import check_case, compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    yield
+    assert attn_fwd_status() == 0
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_named_workload(name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    o, l = run_gpu(q, k, v, w.scale, w.causal)
+    rows = sample_rows(w.Nq, w.sample_rows, w.seed) if w.sample_rows else None
+    mx, mean, dl = compare(o, l, q, k, v, w.scale, w.causal, rows)
+    print(f"{name}: max|dO|={mx:.3e} mean|dO|={mean:.3e} max|dLSE|={dl:.3e}")
+    assert mx <= 2e-2 and mean <= 2e-3 and dl <= 1e-3, (mx, mean, dl)
+
+
+@pytest.mark.parametrize("D", [64, 128, 192, 256, 320, 384, 448, 512, 640, 768, 1024])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dims(D, causal):
+    check_case(1, 2, 1, 200, 200, D, causal, seed=D + causal)
+
+
+@pytest.mark.parametrize("Nq,Nkv", [(1, 1), (1, 300), (63, 63), (128, 128), (129, 129), (257, 100), (100, 257),
+                                    (1000, 1000), (128, 1), (3, 700)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_ragged_lengths(Nq, Nkv, causal, D):
+    check_case(2, 2, 2, Nq, Nkv, D, causal, seed=Nq * 7 + Nkv)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (4, 2), (8, 2), (8, 1), (32, 1), (6, 3)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_ratios(Hq, Hkv, causal):
+    check_case(2, Hq, Hkv, 300, 300, 128, causal, seed=Hq * 10 + Hkv)
+
+
+@pytest.mark.parametrize("D", [128, 512])
+def test_large_scores(D):
+    # scale 1 on amp-2 inputs: scores of order 2*sqrt(D)*2; stresses the running max
+    check_case(1, 2, 2, 256, 600, D, False, seed=5, amp=2.0, scale=1.0)
+
+
+def test_empty_problems():
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 1, 4, 4, 64, 0))
+    o, l = attn_fwd(q[:0], k[:0], v[:0])
+    assert o.shape == (0, 2, 4, 64)
+    o, l = attn_fwd(q[:, :, :0], k, v)
+    assert o.shape == (1, 2, 0, 64)
+    torch.cuda.synchronize()
+
+
+def test_no_keys():
+    q, _, _ = make_qkv(1, 2, 1, 70, 1, 128, 3)
+    k = torch.zeros((1, 1, 0, 128), dtype=torch.bfloat16)
+    o, l = run_gpu(q, k, k.clone(), 0.1, False)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(l))
+
+
+def test_fully_masked_rows():
+    # causal with Nq > Nkv: the first Nq - Nkv rows see no key
+    check_case(1, 2, 2, 300, 100, 128, True, seed=11)
+    q, k, v = make_qkv(1, 1, 1, 300, 100, 64, 12)
+    o, l = run_gpu(q, k, v, 0.125, True)
+    assert torch.all(o[:, :, :200] == 0) and torch.all(torch.isneginf(l[:, :, :200]))
+
+
+def test_deterministic():
+    q, k, v = (t.cuda() for t in make_qkv(2, 4, 2, 777, 777, 128, 21))
+    o1, l1 = attn_fwd(q, k, v, causal=True)
+    o2, l2 = attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_stream_argument():
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 2, 256, 256, 64, 22))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o1, _ = attn_fwd(q, k, v, stream=s)
+    s.synchronize()
+    o2, _ = attn_fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
