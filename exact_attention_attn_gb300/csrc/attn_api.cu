@@ -18,11 +18,15 @@ namespace {
 __device__ int g_status;
 
 constexpr int kMaxDevices = 64;
+// bounded device-side waits give up after this long (a healthy wait lasts
+// microseconds)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 struct DeviceInfo {
   bool ready = false;
   bool arch_ok = false;
   int sm_count = 0;
   int *status = nullptr;
+  int device = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -49,6 +53,7 @@ int device_info(DeviceInfo **out) {
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return record(e);
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return record(e);
     d.arch_ok = (major == 10 && minor == 3);
+    d.device = dev;
     d.sm_count = sms;
     if (d.arch_ok) {
       void *ptr = nullptr;
@@ -83,11 +88,20 @@ void make_plan(const Problem &p, const DeviceInfo &dev, attn_plan *plan) {
     plan->d_slices = 1;
     return;
   }
-  plan->path = ATTN_PATH_SIMT;
+  if (p.Nkv == 0) {  // no keys: every row is O = 0, LSE = -inf
+    plan->path = ATTN_PATH_SIMT;
+    plan->launches = 1;
+    plan->kv_splits = 1;
+    plan->d_slices = (p.D + 255) / 256;
+    plan->grid = (int)(((int64_t)(p.Nq + 63) / 64) * p.B * p.Hq * plan->d_slices);
+    return;
+  }
+  const TcConfig c = tc_config(p.D);
+  plan->path = ATTN_PATH_TC;
   plan->launches = 1;
   plan->kv_splits = 1;
-  plan->d_slices = (p.D + 255) / 256;
-  plan->grid = (int)(((int64_t)(p.Nq + 63) / 64) * p.B * p.Hq * plan->d_slices);
+  plan->d_slices = c.nslices;
+  plan->grid = (int)(((int64_t)(p.Nq + 127) / 128) * p.B * p.Hq * c.nslices);
 }
 
 }  // namespace
@@ -143,7 +157,13 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 
   attn_plan plan;
   make_plan(p, *dev, &plan);
-  cudaError_t e = launch_simt(p, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  switch (plan.path) {
+    case ATTN_PATH_SIMT: e = launch_simt(p, st); break;
+    case ATTN_PATH_TC: e = launch_tc(p, dev->device, kWaitLimitNs, st); break;
+    default: return ATTN_OK;
+  }
   if (e != cudaSuccess) return record(e);
   return ATTN_OK;
 }

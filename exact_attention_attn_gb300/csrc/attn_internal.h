@@ -25,6 +25,23 @@ struct Problem {
 constexpr int kStatusTimeout = -5;
 constexpr int kStatusDevice = -7;
 
+// Shared-memory plan of the tensor-core kernel for head dim D.
+struct TcConfig {
+  int nc;       // 64-column chunks of D
+  int nslices;  // output slices (each <= 256 columns)
+  int vmax;     // chunks in the widest slice
+  int qres;     // Q tile resident in shared memory
+  int kst;      // K-ring depth (16 KB chunks)
+  int vst;      // V-ring depth (slices)
+  uint32_t off_q, off_k, off_v, off_bar;
+  int smem_bytes;
+};
+TcConfig tc_config(int D);
+
+// Tensor-core kernel (tcgen05/TMEM/TMA): every D multiple of 64 up to 1024,
+// Nkv >= 1.  Bounded waits give up after wait_limit_ns.
+cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream);
+
 // Plain CUDA-core kernel: correct for every supported shape; used for the
 // shapes the tensor-core kernel does not take.
 cudaError_t launch_simt(const Problem &p, cudaStream_t stream);

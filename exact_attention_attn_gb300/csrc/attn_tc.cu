@@ -1,0 +1,509 @@
+// Exact attention forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Algorithm: the tiled online softmax of "FlashAttention v1/v2/v3/v4"
+// (lo0.es), sections "El truco que hizo posible todo: online softmax" and
+// "FA4 -- la asimetria de Blackwell": a 128-row query tile visits the key
+// blocks in order; each row keeps a running max m and a running sum l; the
+// output accumulator is rescaled by 2^(m_old - m_new) only when the max grows
+// by more than TAU (conditional rescaling -- exact, because l, P and O all use
+// the same stale max, and P <= 2^TAU stays finite); O is divided by l once at
+// the end.  The N x N scores never leave the chip: S lives in TMEM, P is
+// written back to TMEM as bf16 and fed to the second MMA from there.
+//
+// Large head dims follow the FFPA page ("Split-D and TiledMMA"): the D axis is
+// cut into 64-column chunks staged one at a time through a fixed-size ring,
+// so shared memory holds Br x 64 tiles whatever D is; the output is cut into
+// slices of at most 256 columns (the TMEM accumulator budget), each slice a
+// separate CTA that recomputes the scores.
+//
+// CTA = 6 warps:
+//   warps 0-3  softmax + correction + epilogue, one query row per thread
+//              (warp w may only touch TMEM lanes 32w..32w+31)
+//   warp 4     TMA producer (one thread)
+//   warp 5     TMEM allocator and MMA issuer (one thread)
+//
+// TMEM columns: S [0,128) fp32 scores; P0 [128,192) and P1 [192,256) bf16
+// pairs (double-buffered); O [256, 256+DV) fp32 output slice.
+//
+// Synchronisation (mbarriers; every wait is bounded):
+//   k_full/k_empty, v_full/v_empty   TMA ring <-> MMA
+//   s_full   MMA -> softmax (S_j ready)       s_free  softmax -> MMA (S read)
+//   p_full[2] softmax -> MMA (P_j in TMEM)    o_bar[2] MMA -> softmax (PV_j done)
+// MMA issue order is S_0, S_1, PV_0, S_2, PV_1, ...; tcgen05.commit after S_j
+// therefore also covers PV_{j-2}, which frees P buffer j%2 for P_j and makes
+// every parity wait below unambiguous.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+
+#include <cuda.h>
+
+#include "attn_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;                  // query rows per tile (MMA M)
+constexpr int BN = 128;                  // keys per block (MMA N of S, K of PV)
+constexpr int CHUNK_BYTES = 128 * 128;   // one 128-row x 64-col bf16 tile
+constexpr int THREADS = 192;
+constexpr int WARP_LOAD = 4;
+constexpr int WARP_MMA = 5;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_P0 = 128, TM_P1 = 192, TM_O = 256;
+constexpr float TAU = 8.0f;              // rescale threshold, log2 units
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int MAX_KST = 8, MAX_VST = 2;
+
+struct TcParams {
+  Problem p;
+  int nc;        // contraction chunks = D / 64
+  int nslices;   // output slices
+  int ntiles;    // query tiles per head
+  int kst, vst;  // ring depths (K ring in 16 KB chunks; V ring in slices)
+  int qres;      // Q resident in shared memory (else streamed through the K ring)
+  int vmax;      // chunks in the widest output slice
+  uint32_t off_q, off_k, off_v, off_bar;
+  uint64_t wait_limit_ns;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[MAX_KST];
+  uint64_t k_empty[MAX_KST];
+  uint64_t v_full[MAX_VST];
+  uint64_t v_empty[MAX_VST];
+  uint64_t s_full, s_free;
+  uint64_t p_full[2];
+  uint64_t o_bar[2];
+  uint64_t done;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+__device__ __forceinline__ void raise_abort(Bars *bars, int *status) {
+  atomicCAS(status, 0, kStatusTimeout);
+  *reinterpret_cast<volatile int *>(&bars->abort) = 1;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t *sq = smem + prm.off_q;
+  uint8_t *sk = smem + prm.off_k;
+  uint8_t *sv = smem + prm.off_v;
+  Bars *bars = reinterpret_cast<Bars *>(smem + prm.off_bar);
+  volatile int *abortf = &bars->abort;
+
+  const Problem &p = prm.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint64_t limit = prm.wait_limit_ns;
+
+  // ---- work unit: output slice fastest, then (b, hq), then query tile
+  //      (heaviest causal tiles first)
+  int bid = blockIdx.x;
+  const int slice = bid % prm.nslices;
+  bid /= prm.nslices;
+  const int BH = p.B * p.Hq;
+  const int bh = bid % BH;
+  const int t = bid / BH;
+  const int tile = p.causal ? (prm.ntiles - 1 - t) : t;
+  const int b = bh / p.Hq, hq = bh % p.Hq;
+  const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
+  const int q0 = tile * BM;
+  const int sbase = prm.nc / prm.nslices, srem = prm.nc % prm.nslices;
+  const int s_chunks = sbase + (slice < srem ? 1 : 0);
+  const int s_c0 = slice * sbase + (slice < srem ? slice : srem);
+  const int DV = s_chunks * 64;
+  const int shift = p.Nkv - p.Nq;  // bottom-right causal alignment
+  int kv_end = p.Nkv;
+  if (p.causal) kv_end = max(0, min(p.Nkv, q0 + BM - 1 + shift + 1));
+  const int nblk = (kv_end + BN - 1) / BN;
+
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < prm.kst; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < prm.vst; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 4 * 32);
+    mbar_init(&bars->p_full[0], 4 * 32);
+    mbar_init(&bars->p_full[1], 4 * 32);
+    mbar_init(&bars->o_bar[0], 1);
+    mbar_init(&bars->o_bar[1], 1);
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(&bars->tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == WARP_LOAD) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nblk > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t kctr = 0, vctr = 0;
+      bool ok = true;
+      if (prm.qres) {
+        mbar_arrive_expect_tx(&bars->q_full, prm.nc * CHUNK_BYTES);
+        for (int c = 0; c < prm.nc; ++c) tma_load_3d(sq + c * CHUNK_BYTES, &tm_q, &bars->q_full, c * 64, q0, bh);
+      }
+      for (int j = 0; j < nblk && ok; ++j) {
+        for (int c = 0; c < prm.nc && ok; ++c) {
+          if (!prm.qres) {
+            const int s = kctr % prm.kst;
+            if (!mbar_wait(&bars->k_empty[s], ((kctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+            mbar_arrive_expect_tx(&bars->k_full[s], CHUNK_BYTES);
+            tma_load_3d(sk + s * CHUNK_BYTES, &tm_q, &bars->k_full[s], c * 64, q0, bh);
+            ++kctr;
+          }
+          const int s = kctr % prm.kst;
+          if (!mbar_wait(&bars->k_empty[s], ((kctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->k_full[s], CHUNK_BYTES);
+          tma_load_3d(sk + s * CHUNK_BYTES, &tm_k, &bars->k_full[s], c * 64, j * BN, bkv);
+          ++kctr;
+        }
+        if (!ok) break;
+        const int vs = vctr % prm.vst;
+        if (!mbar_wait(&bars->v_empty[vs], ((vctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bars->v_full[vs], s_chunks * CHUNK_BYTES);
+        uint8_t *vdst = sv + vs * (prm.vmax * CHUNK_BYTES);
+        for (int c = 0; c < s_chunks; ++c)
+          tma_load_3d(vdst + c * CHUNK_BYTES, &tm_v, &bars->v_full[vs], (s_c0 + c) * 64, j * BN, bkv);
+        ++vctr;
+      }
+      if (!ok) raise_abort(bars, p.status);
+      // drain: every copy this thread issued must land before the CTA exits
+      if (prm.qres) mbar_wait_drain(&bars->q_full, 0, limit);
+      const uint32_t kn = kctr < (uint32_t)prm.kst ? kctr : (uint32_t)prm.kst;
+      for (uint32_t i = kctr - kn; i < kctr; ++i) mbar_wait_drain(&bars->k_full[i % prm.kst], (i / prm.kst) & 1, limit);
+      const uint32_t vn = vctr < (uint32_t)prm.vst ? vctr : (uint32_t)prm.vst;
+      for (uint32_t i = vctr - vn; i < vctr; ++i) mbar_wait_drain(&bars->v_full[i % prm.vst], (i / prm.vst) & 1, limit);
+    }
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nblk > 0) {
+      const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16(BM, DV, 0, 1);
+      const uint32_t sq_addr = smem_u32(sq), sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
+      uint32_t kctr = 0, vctr = 0;
+      bool ok = true;
+      if (prm.qres) ok = mbar_wait(&bars->q_full, 0, abortf, limit);
+      auto issue_s = [&]() -> bool {
+        for (int c = 0; c < prm.nc; ++c) {
+          uint32_t qaddr;
+          int qslot = -1;
+          if (prm.qres) {
+            qaddr = sq_addr + c * CHUNK_BYTES;
+          } else {
+            qslot = kctr % prm.kst;
+            if (!mbar_wait(&bars->k_full[qslot], (kctr / prm.kst) & 1, abortf, limit)) return false;
+            qaddr = sk_addr + qslot * CHUNK_BYTES;
+            ++kctr;
+          }
+          const int ks = kctr % prm.kst;
+          if (!mbar_wait(&bars->k_full[ks], (kctr / prm.kst) & 1, abortf, limit)) return false;
+          const uint32_t kaddr = sk_addr + ks * CHUNK_BYTES;
+          ++kctr;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + TM_S, smem_desc(qaddr + kk * 32, 16, 1024), smem_desc(kaddr + kk * 32, 16, 1024), idesc_s,
+                   (c | kk) != 0);
+          mma_commit(&bars->k_empty[ks]);
+          if (qslot >= 0) mma_commit(&bars->k_empty[qslot]);
+        }
+        mma_commit(&bars->s_full);
+        return true;
+      };
+      if (ok) ok = issue_s();
+      for (int j = 0; j < nblk && ok; ++j) {
+        if (j + 1 < nblk) {
+          if (!mbar_wait(&bars->s_free, j & 1, abortf, limit)) { ok = false; break; }
+          tc_fence_after();
+          if (!issue_s()) { ok = false; break; }
+        }
+        if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abortf, limit)) { ok = false; break; }
+        const int vs = vctr % prm.vst;
+        if (!mbar_wait(&bars->v_full[vs], (vctr / prm.vst) & 1, abortf, limit)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t vaddr = sv_addr + vs * (prm.vmax * CHUNK_BYTES);
+        const uint32_t pcol = (j & 1) ? TM_P1 : TM_P0;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + TM_O, tmem + pcol + kk * 8, smem_desc(vaddr + kk * 2048, CHUNK_BYTES, 1024), idesc_pv,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->v_empty[vs]);
+        ++vctr;
+        mma_commit(&bars->o_bar[j & 1]);
+      }
+      if (!ok) raise_abort(bars, p.status);
+      // every MMA this thread issued completes before TMEM is released
+      mma_commit(&bars->done);
+      if (!mbar_wait_drain(&bars->done, 0, limit)) raise_abort(bars, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int row = tid;  // 0..127
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int qi = q0 + row;
+    const int vis_end = p.causal ? min(p.Nkv, qi + shift + 1) : p.Nkv;  // keys [0, vis_end) are visible
+    const float sl2 = p.scale * kLog2e;
+    float m_use = -INFINITY, l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < nblk; ++j) {
+      // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, abortf, limit))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[BN / 32][32];
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tmem + lane_base + TM_S + cc * 32, sr[cc]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) reg_fence32(sr[cc]);
+      float x[BN];
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[cc * 32 + i] = __uint_as_float(sr[cc][i]);
+      tc_fence_before();
+      mbar_arrive(&bars->s_free);
+
+      // scale to log2 units, mask, block max
+      const int kbase = j * BN;
+      float mblk = -INFINITY;
+      if (kbase + BN <= vis_end) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          x[c] *= sl2;
+          mblk = fmaxf(mblk, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          x[c] = (kbase + c < vis_end) ? x[c] * sl2 : -INFINITY;
+          mblk = fmaxf(mblk, x[c]);
+        }
+      }
+      const float m_new = fmaxf(m_use, mblk);
+      const bool need = m_new > m_use + TAU;
+      if (__any_sync(0xffffffffu, need)) {
+        // the whole warp moves to its new maxima (exact for any choice)
+        const float alpha = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m_new);
+        if (j > 0) {
+          const int pj = j - 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_bar[pj & 1], (pj >> 1) & 1, abortf, limit))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int cc = 0; cc < DV / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + TM_O + cc * 32, r);
+            tmem_wait_ld();
+            reg_fence32(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tmem + lane_base + TM_O + cc * 32, r);
+          }
+          tmem_wait_st();
+        }
+        l *= alpha;
+        m_use = m_new;
+      }
+      const float mu = (m_use == -INFINITY) ? 0.f : m_use;
+      const uint32_t pcol = (j & 1) ? TM_P1 : TM_P0;
+      float lsum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(x[h * 64 + 2 * i] - mu);
+          const float p1 = ex2_approx(x[h * 64 + 2 * i + 1] - mu);
+          lsum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tmem + lane_base + pcol + h * 32, pk);
+      }
+      l += lsum;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[j & 1]);
+    }
+
+    if (!ok) raise_abort(bars, p.status);
+    // ---- epilogue: O / l -> bf16, LSE
+    __nv_bfloat16 *orow = p.o + ((int64_t)bh * p.Nq + qi) * p.D + s_c0 * 64;
+    if (ok && nblk > 0) {
+      const int last = nblk - 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_bar[last & 1], (last >> 1) & 1, abortf, limit))) {
+        raise_abort(bars, p.status);
+        ok = false;
+      }
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      for (int cc = 0; cc < DV / 32; ++cc) {
+        uint32_t r[32];
+        if (nblk > 0) {
+          tmem_ld32(tmem + lane_base + TM_O + cc * 32, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (qi < p.Nq) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
+            dst[v4] = w;
+          }
+        }
+      }
+      if (slice == 0 && qi < p.Nq)
+        p.lse[(int64_t)bh * p.Nq + qi] = (m_use == -INFINITY || !(l > 0.f)) ? -INFINITY : (m_use + log2f(l)) * kLn2;
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    cudaDriverEntryPointQueryResult q;
+    void *ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    tried = true;
+  }
+  return fn;
+}
+
+// [planes, rows, cols] bf16 tensor, boxes of 128 rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int cols, int rows, int planes) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * rows * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kSmemMax = 232448;  // opt-in dynamic shared memory per block on sm_100-family
+constexpr int kSmemReserve = 2048;
+constexpr int kMaxDevicesTc = 64;
+
+}  // namespace
+
+TcConfig tc_config(int D) {
+  TcConfig c;
+  c.nc = D / 64;
+  c.nslices = (D + 255) / 256;
+  c.vmax = (c.nc + c.nslices - 1) / c.nslices;
+  const int avail = kSmemMax - kSmemReserve;
+  const int qb = c.nc * CHUNK_BYTES, vb = c.vmax * CHUNK_BYTES;
+  c.qres = qb + 2 * CHUNK_BYTES + vb <= avail;
+  if (c.qres) {
+    c.vst = (avail - qb - 2 * CHUNK_BYTES >= 2 * vb) ? 2 : 1;
+    c.kst = (avail - qb - c.vst * vb) / CHUNK_BYTES;
+  } else {
+    c.vst = (avail - 4 * CHUNK_BYTES >= 2 * vb) ? 2 : 1;
+    c.kst = (avail - c.vst * vb) / CHUNK_BYTES;
+    c.kst &= ~1;
+  }
+  if (c.kst > MAX_KST) c.kst = MAX_KST;
+  c.off_q = 0;
+  c.off_k = c.qres ? qb : 0;
+  c.off_v = c.off_k + c.kst * CHUNK_BYTES;
+  c.off_bar = c.off_v + c.vst * vb;
+  c.smem_bytes = c.off_bar + (int)sizeof(Bars) + 1024;  // + alignment slack
+  return c;
+}
+
+cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
+  static_assert(sizeof(Bars) <= kSmemReserve - 1024, "barrier block too large");
+  const TcConfig c = tc_config(p.D);
+  if (c.kst < 2 || c.smem_bytes > kSmemMax) return cudaErrorInvalidConfiguration;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq)) return cudaErrorInvalidValue;
+  if (!make_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
+  if (!make_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
+  TcParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.p = p;
+  prm.nc = c.nc;
+  prm.nslices = c.nslices;
+  prm.ntiles = (p.Nq + BM - 1) / BM;
+  prm.kst = c.kst;
+  prm.vst = c.vst;
+  prm.qres = c.qres;
+  prm.vmax = c.vmax;
+  prm.off_q = c.off_q;
+  prm.off_k = c.off_k;
+  prm.off_v = c.off_v;
+  prm.off_bar = c.off_bar;
+  prm.wait_limit_ns = wait_limit_ns;
+  const int64_t grid = (int64_t)prm.ntiles * p.B * p.Hq * c.nslices;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // the opt-in shared-memory limit is a per-device function attribute: raise
+  // it to the maximum once per device
+  static std::atomic<int> attr_set[kMaxDevicesTc];
+  if (device < 0 || device >= kMaxDevicesTc) return cudaErrorInvalidDevice;
+  if (!attr_set[device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_set[device].store(1, std::memory_order_release);
+  }
+  attn_tc_kernel<<<(unsigned)grid, THREADS, c.smem_bytes, stream>>>(tq, tk, tv, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace attn
