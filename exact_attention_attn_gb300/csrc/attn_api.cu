@@ -96,12 +96,17 @@ void make_plan(const Problem &p, const DeviceInfo &dev, attn_plan *plan) {
     plan->grid = (int)(((int64_t)(p.Nq + 63) / 64) * p.B * p.Hq * plan->d_slices);
     return;
   }
-  const TcConfig c = tc_config(p.D);
   plan->path = ATTN_PATH_TC;
   plan->launches = 1;
   plan->kv_splits = 1;
-  plan->d_slices = c.nslices;
-  plan->grid = (int)(((int64_t)(p.Nq + 127) / 128) * p.B * p.Hq * c.nslices);
+  if (tc2_supports(p.D)) {
+    plan->d_slices = 1;
+    plan->grid = (int)((((int64_t)(p.Nq + 127) / 128 + 1) / 2) * p.B * p.Hq);
+  } else {
+    const TcConfig c = tc_config(p.D);
+    plan->d_slices = c.nslices;
+    plan->grid = (int)(((int64_t)(p.Nq + 127) / 128) * p.B * p.Hq * c.nslices);
+  }
 }
 
 }  // namespace
@@ -161,7 +166,9 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
   cudaError_t e = cudaSuccess;
   switch (plan.path) {
     case ATTN_PATH_SIMT: e = launch_simt(p, st); break;
-    case ATTN_PATH_TC: e = launch_tc(p, dev->device, kWaitLimitNs, st); break;
+    case ATTN_PATH_TC:
+      e = tc2_supports(p.D) ? launch_tc2(p, dev->device, kWaitLimitNs, st) : launch_tc(p, dev->device, kWaitLimitNs, st);
+      break;
     default: return ATTN_OK;
   }
   if (e != cudaSuccess) return record(e);

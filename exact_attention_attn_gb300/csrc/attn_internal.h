@@ -2,6 +2,7 @@
 // translation units of libattn_gb300.so.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -25,6 +26,10 @@ struct Problem {
 constexpr int kStatusTimeout = -5;
 constexpr int kStatusDevice = -7;
 
+// TMA map of a [planes, rows, cols] bf16 tensor (cols contiguous) with
+// 128-row x 64-column boxes and the 128-byte swizzle.  False on failure.
+bool make_tile_map(CUtensorMap *m, const void *base, int cols, int rows, int planes);
+
 // Shared-memory plan of the tensor-core kernel for head dim D.
 struct TcConfig {
   int nc;       // 64-column chunks of D
@@ -41,6 +46,10 @@ TcConfig tc_config(int D);
 // Tensor-core kernel (tcgen05/TMEM/TMA): every D multiple of 64 up to 1024,
 // Nkv >= 1.  Bounded waits give up after wait_limit_ns.
 cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream);
+
+// Two-tile ping-pong tensor-core kernel for head dims 64 and 128.
+bool tc2_supports(int D);
+cudaError_t launch_tc2(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream);
 
 // Plain CUDA-core kernel: correct for every supported shape; used for the
 // shapes the tensor-core kernel does not take.

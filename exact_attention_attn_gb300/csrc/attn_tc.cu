@@ -405,38 +405,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    cudaDriverEntryPointQueryResult q;
-    void *ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    tried = true;
-  }
-  return fn;
-}
-
-// [planes, rows, cols] bf16 tensor, boxes of 128 rows x 64 columns, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, int cols, int rows, int planes) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
-  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * rows * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr int kSmemMax = 232448;  // opt-in dynamic shared memory per block on sm_100-family
 constexpr int kSmemReserve = 2048;
 constexpr int kMaxDevicesTc = 64;
@@ -473,9 +441,9 @@ cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cuda
   const TcConfig c = tc_config(p.D);
   if (c.kst < 2 || c.smem_bytes > kSmemMax) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq)) return cudaErrorInvalidValue;
-  if (!make_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
-  if (!make_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
+  if (!make_tile_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq)) return cudaErrorInvalidValue;
+  if (!make_tile_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
+  if (!make_tile_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.p = p;

@@ -1,0 +1,435 @@
+// Exact attention forward for head dims 64 and 128: two 128-row query tiles
+// per CTA in ping-pong on the sm_103a tensor cores.
+//
+// The online softmax is the one of "FlashAttention v1/v2/v3/v4" (lo0.es),
+// "El truco que hizo posible todo: online softmax", with the conditional
+// rescaling of its "FA4 -- la asimetria de Blackwell" section (rescale only
+// when the running max grows by more than TAU in log2 units).  The overlap
+// follows the producer/consumer warp specialisation and the two-warpgroup
+// ping-pong of its "FA3 -- el momento Hopper" section, rebuilt on tcgen05:
+// while warpgroup 0 turns S0 into P0, the tensor core runs P1 V and Q1 K^T
+// for the other tile, and the other way round.  Both tiles share every K and
+// V block loaded into shared memory.
+//
+// CTA = 10 warps:
+//   warps 0-3 softmax + epilogue of tile 0, warps 4-7 of tile 1
+//   (one query row per thread; warp w touches TMEM lanes 32(w%4)..+31)
+//   warp 8  TMA producer (one thread)
+//   warp 9  TMEM allocator and MMA issuer (one thread)
+//
+// TMEM columns: S_t at [128t, 128t+128) fp32, with P_t (bf16 pairs) written
+// over its first 64 columns; O_t at [256 + 128t, 256 + 128t + D) fp32.
+//
+// MMA issue order per block j: PV0_j, S0_{j+1}, PV1_j, S1_{j+1}.  Both the
+// overwrite of P_t by S_t,{j+1} and the rescale of O_t rely on tcgen05.mma
+// executing in issue order and on tcgen05.commit tracking every earlier MMA of
+// the issuing thread: the commit that announces S_t,j also covers PV_t,{j-1},
+// so O_t may be rescaled as soon as S_t,j is visible.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "attn_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128, BN = 128;
+constexpr int CHUNK_BYTES = 128 * 128;
+constexpr int THREADS = 320;
+constexpr int WARP_LOAD = 8, WARP_MMA = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float TAU = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int MAX_KST = 8, MAX_VST = 3;
+constexpr int kSmemMax = 232448;
+
+struct Params2 {
+  Problem p;
+  int npairs;        // tile pairs per head
+  int kst, vst;      // K ring (16 KB chunks), V ring (blocks)
+  uint32_t off_k, off_v, off_bar;
+  uint64_t wait_limit_ns;
+};
+
+struct Bars2 {
+  uint64_t q_full;
+  uint64_t k_full[MAX_KST];
+  uint64_t k_empty[MAX_KST];
+  uint64_t v_full[MAX_VST];
+  uint64_t v_empty[MAX_VST];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t done;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+__device__ __forceinline__ void raise_abort(Bars2 *bars, int *status) {
+  atomicCAS(status, 0, kStatusTimeout);
+  *reinterpret_cast<volatile int *>(&bars->abort) = 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params2 prm) {
+  constexpr int NC = D / 64;  // 64-column chunks per row
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t *sq = smem;  // Q0 chunks then Q1 chunks
+  uint8_t *sk = smem + prm.off_k;
+  uint8_t *sv = smem + prm.off_v;
+  Bars2 *bars = reinterpret_cast<Bars2 *>(smem + prm.off_bar);
+  volatile int *abortf = &bars->abort;
+
+  const Problem &p = prm.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint64_t limit = prm.wait_limit_ns;
+
+  // ---- work unit: (b, hq) fastest, then tile pair (heaviest causal pairs first)
+  const int BH = p.B * p.Hq;
+  const int bh = blockIdx.x % BH;
+  const int t_idx = blockIdx.x / BH;
+  const int pair = p.causal ? (prm.npairs - 1 - t_idx) : t_idx;
+  const int b = bh / p.Hq, hq = bh % p.Hq;
+  const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
+  const int shift = p.Nkv - p.Nq;
+  int nblk_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int q0 = pair * 2 * BM + t * BM;
+    int kv_end = p.Nkv;
+    if (p.causal) kv_end = max(0, min(p.Nkv, q0 + BM - 1 + shift + 1));
+    nblk_t[t] = (q0 < p.Nq) ? (kv_end + BN - 1) / BN : 0;
+  }
+  const int nblk = max(nblk_t[0], nblk_t[1]);
+
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < prm.kst; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < prm.vst; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->o_done[t], 1);
+    }
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(&bars->tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == WARP_LOAD) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nblk > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int ntq = nblk_t[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bars->q_full, ntq * NC * CHUNK_BYTES);
+      for (int t = 0; t < ntq; ++t)
+        for (int c = 0; c < NC; ++c)
+          tma_load_3d(sq + (t * NC + c) * CHUNK_BYTES, &tm_q, &bars->q_full, c * 64, pair * 2 * BM + t * BM, bh);
+      uint32_t kctr = 0, vctr = 0;
+      bool ok = true;
+      for (int j = 0; j < nblk && ok; ++j) {
+        for (int c = 0; c < NC; ++c) {
+          const int s = kctr % prm.kst;
+          if (!mbar_wait(&bars->k_empty[s], ((kctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->k_full[s], CHUNK_BYTES);
+          tma_load_3d(sk + s * CHUNK_BYTES, &tm_k, &bars->k_full[s], c * 64, j * BN, bkv);
+          ++kctr;
+        }
+        if (!ok) break;
+        const int vs = vctr % prm.vst;
+        if (!mbar_wait(&bars->v_empty[vs], ((vctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bars->v_full[vs], NC * CHUNK_BYTES);
+        for (int c = 0; c < NC; ++c)
+          tma_load_3d(sv + (vs * NC + c) * CHUNK_BYTES, &tm_v, &bars->v_full[vs], c * 64, j * BN, bkv);
+        ++vctr;
+      }
+      if (!ok) raise_abort(bars, p.status);
+      mbar_wait_drain(&bars->q_full, 0, limit);
+      const uint32_t kn = kctr < (uint32_t)prm.kst ? kctr : (uint32_t)prm.kst;
+      for (uint32_t i = kctr - kn; i < kctr; ++i) mbar_wait_drain(&bars->k_full[i % prm.kst], (i / prm.kst) & 1, limit);
+      const uint32_t vn = vctr < (uint32_t)prm.vst ? vctr : (uint32_t)prm.vst;
+      for (uint32_t i = vctr - vn; i < vctr; ++i) mbar_wait_drain(&bars->v_full[i % prm.vst], (i / prm.vst) & 1, limit);
+    }
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nblk > 0) {
+      const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
+      const uint32_t sq_addr = smem_u32(sq), sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
+      bool ok = mbar_wait(&bars->q_full, 0, abortf, limit);
+      // S_t,blk = Q_t K_blk^T; K chunks of block blk sit in ring slots (blk*NC + c) % kst
+      auto issue_s = [&](int t, int blk, bool wait_full, bool release) -> bool {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const uint32_t idx = (uint32_t)(blk * NC + c);
+          const int s = idx % prm.kst;
+          if (wait_full && !mbar_wait(&bars->k_full[s], (idx / prm.kst) & 1, abortf, limit)) return false;
+          tc_fence_after();
+          const uint32_t qaddr = sq_addr + (t * NC + c) * CHUNK_BYTES;
+          const uint32_t kaddr = sk_addr + s * CHUNK_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + 128 * t, smem_desc(qaddr + kk * 32, 16, 1024), smem_desc(kaddr + kk * 32, 16, 1024),
+                   idesc_s, (c | kk) != 0);
+          if (release) mma_commit(&bars->k_empty[s]);
+        }
+        mma_commit(&bars->s_full[t]);
+        return true;
+      };
+      auto act = [&](int t, int j) { return j < nblk_t[t]; };
+      if (ok && act(0, 0)) ok = issue_s(0, 0, true, !act(1, 0));
+      if (ok && act(1, 0)) ok = issue_s(1, 0, !act(0, 0), true);
+      for (int j = 0; j < nblk && ok; ++j) {
+        const int vs = j % prm.vst;
+        if (!mbar_wait(&bars->v_full[vs], (j / prm.vst) & 1, abortf, limit)) { ok = false; break; }
+        const uint32_t vaddr = sv_addr + vs * NC * CHUNK_BYTES;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!act(t, j)) continue;
+          if (!mbar_wait(&bars->p_full[t], j & 1, abortf, limit)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, smem_desc(vaddr + kk * 2048, CHUNK_BYTES, 1024),
+                   idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          if (j == nblk_t[t] - 1) mma_commit(&bars->o_done[t]);
+          if (act(t, j + 1)) {
+            const bool first = (t == 0) || !act(0, j + 1);
+            const bool last = (t == 1) || !act(1, j + 1);
+            if (!issue_s(t, j + 1, first, last)) { ok = false; break; }
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bars->v_empty[vs]);
+      }
+      if (!ok) raise_abort(bars, p.status);
+      mma_commit(&bars->done);
+      if (!mbar_wait_drain(&bars->done, 0, limit)) raise_abort(bars, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int t = warp >> 2;          // tile of this warpgroup
+    const int row = tid & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + 128 * t;
+    const uint32_t tO = tmem + lane_base + 256 + 128 * t;
+    const int qi = pair * 2 * BM + t * BM + row;
+    const int nb = nblk_t[t];
+    const int vis_end = p.causal ? min(p.Nkv, qi + shift + 1) : p.Nkv;
+    const float sl2 = p.scale * kLog2e;
+    const bool pos = sl2 > 0.f;  // uniform across the CTA
+    float m_use = -INFINITY, l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < nb; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abortf, limit))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      const int kbase = j * BN;
+      if (kbase + BN > vis_end) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (kbase + c >= vis_end) x[c] = pos ? -INFINITY : INFINITY;
+      }
+      // block max of the scaled scores, four independent chains
+      float mx[4];
+      if (pos) {
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) mx[k4] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN; c += 4)
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) mx[k4] = fmaxf(mx[k4], x[c + k4]);
+      } else {
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) mx[k4] = INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN; c += 4)
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) mx[k4] = fminf(mx[k4], x[c + k4]);
+      }
+      const float ext = pos ? fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]))
+                            : fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3]));
+      // ext*sl2 is the block max of the scaled scores; masked-only rows give -inf
+      const float mblk = (ext == (pos ? -INFINITY : INFINITY)) ? -INFINITY : (sl2 == 0.f ? 0.f : ext * sl2);
+      const float m_new = fmaxf(m_use, mblk);
+      if (__any_sync(0xffffffffu, m_new > m_use + TAU)) {
+        const float alpha = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m_new);
+        if (j > 0) {
+          // PV_t,{j-1} is complete: the commit that announced S_t,j covers it
+#pragma unroll 1
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t r[16];
+            tmem_ld16(tO + cc * 16, r);
+            tmem_wait_ld();
+            reg_fence16(r);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st16(tO + cc * 16, r);
+          }
+        }
+        l *= alpha;
+        m_use = m_new;
+      }
+      const float mu = (m_use == -INFINITY) ? 0.f : m_use;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = x[h * 32 + 2 * i], bb = x[h * 32 + 2 * i + 1];
+          // masked entries hold -inf (or +inf when scale < 0) and give exactly 0
+          float p0, p1;
+          if (pos) {
+            p0 = ex2_approx(fmaf(a, sl2, -mu));
+            p1 = ex2_approx(fmaf(bb, sl2, -mu));
+          } else {
+            p0 = (a == INFINITY) ? 0.f : ex2_approx(fmaf(a, sl2, -mu));
+            p1 = (bb == INFINITY) ? 0.f : ex2_approx(fmaf(bb, sl2, -mu));
+          }
+          ls[i & 3] += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + h * 16, pk);
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[t]);
+    }
+    if (!ok) raise_abort(bars, p.status);
+
+    // ---- epilogue
+    if (ok && nb > 0) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], 0, abortf, limit))) {
+        raise_abort(bars, p.status);
+        ok = false;
+      }
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      __nv_bfloat16 *orow = p.o + ((int64_t)bh * p.Nq + qi) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        if (nb > 0) {
+          tmem_ld32(tO + cc * 32, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (qi < p.Nq) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
+            dst[v4] = w;
+          }
+        }
+      }
+      if (qi < p.Nq)
+        p.lse[(int64_t)bh * p.Nq + qi] = (m_use == -INFINITY || !(l > 0.f)) ? -INFINITY : (m_use + log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
+  constexpr int NC = D / 64;
+  const int avail = kSmemMax - 2048;
+  const int qb = 2 * NC * CHUNK_BYTES, vb = NC * CHUNK_BYTES;
+  int vst = 2;
+  int kst = (avail - qb - vst * vb) / CHUNK_BYTES;
+  if (kst > MAX_KST) kst = MAX_KST;
+  if (kst < NC) return cudaErrorInvalidConfiguration;
+  Params2 prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.p = p;
+  prm.npairs = ((p.Nq + BM - 1) / BM + 1) / 2;
+  prm.kst = kst;
+  prm.vst = vst;
+  prm.off_k = qb;
+  prm.off_v = qb + kst * CHUNK_BYTES;
+  prm.off_bar = prm.off_v + vst * vb;
+  prm.wait_limit_ns = wait_limit_ns;
+  const int smem = prm.off_bar + (int)sizeof(Bars2) + 1024;
+  if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
+  CUtensorMap tq, tk, tv;
+  if (!make_tile_map(&tq, p.q, D, p.Nq, p.B * p.Hq)) return cudaErrorInvalidValue;
+  if (!make_tile_map(&tk, p.k, D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
+  if (!make_tile_map(&tv, p.v, D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
+  static std::atomic<int> attr_set[64];
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_set[device].store(1, std::memory_order_release);
+  }
+  const int64_t grid = (int64_t)prm.npairs * p.B * p.Hq;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  attn_tc2_kernel<D><<<(unsigned)grid, THREADS, smem, stream>>>(tq, tk, tv, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc2_supports(int D) { return D == 64 || D == 128; }
+
+cudaError_t launch_tc2(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
+  if (p.D == 64) return launch_tc2_d<64>(p, device, wait_limit_ns, stream);
+  if (p.D == 128) return launch_tc2_d<128>(p, device, wait_limit_ns, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn
