@@ -30,6 +30,12 @@ constexpr int kStatusDevice = -7;
 // 128-row x 64-column boxes and the 128-byte swizzle.  False on failure.
 bool make_tile_map(CUtensorMap *m, const void *base, int cols, int rows, int planes);
 
+// TMA map of the same tensor whose box is box_rows rows x all of its columns,
+// landing in shared memory as cols/64 consecutive [box_rows x 64] chunks with
+// the 128-byte swizzle.  One copy moves a whole K or V block: large copies
+// keep more bytes in flight per TMA operation.
+bool make_block_map(CUtensorMap *m, const void *base, int cols, int rows, int planes, int box_rows);
+
 // Shared-memory plan of the tensor-core kernel for head dim D.
 struct TcConfig {
   int nc;       // 64-column chunks of D

@@ -11,11 +11,12 @@
 // for the other tile, and the other way round.  Both tiles share every K and
 // V block loaded into shared memory.
 //
-// CTA = 10 warps:
+// CTA = 11 warps:
 //   warps 0-3 softmax + epilogue of tile 0, warps 4-7 of tile 1
 //   (one query row per thread; warp w touches TMEM lanes 32(w%4)..+31)
-//   warp 8  TMA producer (one thread)
+//   warp 8  TMA producer of Q and K (one thread)
 //   warp 9  TMEM allocator and MMA issuer (one thread)
+//   warp 10 TMA producer of V (one thread)
 //
 // TMEM columns: S_t at [128t, 128t+128) fp32, with P_t (bf16 pairs) written
 // over its first 64 columns; O_t at [256 + 128t, 256 + 128t + D) fp32.
@@ -33,6 +34,23 @@
 #include "attn_internal.h"
 #include "sm100_ptx.cuh"
 
+// Optional per-role timestamps (clock64) for a few CTAs, compiled in only
+// when ATTN_TRACE is defined: ATTN_TRACE_EV(row, col) stores into the
+// caller-provided buffer attn_trace_buf[cta][16][64].
+#ifdef ATTN_TRACE
+__device__ long long *attn_trace_buf;
+#define ATTN_TRACE_EV(row, col)                                                                         \
+  do {                                                                                                  \
+    const long long _t = clock64();                                                                     \
+    long long *_b = attn_trace_buf;                                                                     \
+    if (_b && blockIdx.x < 8 && (col) < 64) _b[((long long)blockIdx.x * 16 + (row)) * 64 + (col)] = _t; \
+  } while (0)
+#else
+#define ATTN_TRACE_EV(row, col) \
+  do {                          \
+  } while (0)
+#endif
+
 namespace attn {
 namespace {
 
@@ -40,8 +58,8 @@ using namespace ptx;
 
 constexpr int BM = 128, BN = 128;
 constexpr int CHUNK_BYTES = 128 * 128;
-constexpr int THREADS = 320;
-constexpr int WARP_LOAD = 8, WARP_MMA = 9;
+constexpr int THREADS = 352;
+constexpr int WARP_LOAD_K = 8, WARP_LOAD_V = 10, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float TAU = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -140,41 +158,49 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
-  if (warp == WARP_LOAD) {
-    // ------------------------------------------------------------ producer
+  if (warp == WARP_LOAD_K || warp == WARP_LOAD_V) {
+    // ------------------------------------------------------------ producers
+    // Two independent producer threads (Q+K and V), each moving a whole
+    // 128-key block (all D/64 chunks) with one 4-D TMA copy.
     if (lane == 0 && nblk > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const int ntq = nblk_t[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&bars->q_full, ntq * NC * CHUNK_BYTES);
-      for (int t = 0; t < ntq; ++t)
-        for (int c = 0; c < NC; ++c)
-          tma_load_3d(sq + (t * NC + c) * CHUNK_BYTES, &tm_q, &bars->q_full, c * 64, pair * 2 * BM + t * BM, bh);
-      uint32_t kctr = 0, vctr = 0;
+      const bool is_k = warp == WARP_LOAD_K;
+      uint32_t ctr = 0;
       bool ok = true;
-      for (int j = 0; j < nblk && ok; ++j) {
-        for (int c = 0; c < NC; ++c) {
-          const int s = kctr % prm.kst;
-          if (!mbar_wait(&bars->k_empty[s], ((kctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->k_full[s], CHUNK_BYTES);
-          tma_load_3d(sk + s * CHUNK_BYTES, &tm_k, &bars->k_full[s], c * 64, j * BN, bkv);
-          ++kctr;
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        // both query tiles (256 rows, zero-filled past Nq) in one copy
+        mbar_arrive_expect_tx(&bars->q_full, 2 * NC * CHUNK_BYTES);
+        tma_load_4d(sq, &tm_q, &bars->q_full, 0, pair * 2 * BM, 0, bh);
+        for (int j = 0; j < nblk; ++j) {
+          const int s = ctr % prm.kst;
+          if (!mbar_wait(&bars->k_empty[s], ((ctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->k_full[s], NC * CHUNK_BYTES);
+          tma_load_4d(sk + s * NC * CHUNK_BYTES, &tm_k, &bars->k_full[s], 0, j * BN, 0, bkv);
+          ATTN_TRACE_EV(13, j);
+          ++ctr;
         }
-        if (!ok) break;
-        const int vs = vctr % prm.vst;
-        if (!mbar_wait(&bars->v_empty[vs], ((vctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars->v_full[vs], NC * CHUNK_BYTES);
-        for (int c = 0; c < NC; ++c)
-          tma_load_3d(sv + (vs * NC + c) * CHUNK_BYTES, &tm_v, &bars->v_full[vs], c * 64, j * BN, bkv);
-        ++vctr;
+      } else {
+        tma_prefetch_desc(&tm_v);
+        for (int j = 0; j < nblk; ++j) {
+          const int vs = ctr % prm.vst;
+          if (!mbar_wait(&bars->v_empty[vs], ((ctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->v_full[vs], NC * CHUNK_BYTES);
+          tma_load_4d(sv + vs * NC * CHUNK_BYTES, &tm_v, &bars->v_full[vs], 0, j * BN, 0, bkv);
+          ATTN_TRACE_EV(14, j);
+          ++ctr;
+        }
       }
       if (!ok) raise_abort(bars, p.status);
-      mbar_wait_drain(&bars->q_full, 0, limit);
-      const uint32_t kn = kctr < (uint32_t)prm.kst ? kctr : (uint32_t)prm.kst;
-      for (uint32_t i = kctr - kn; i < kctr; ++i) mbar_wait_drain(&bars->k_full[i % prm.kst], (i / prm.kst) & 1, limit);
-      const uint32_t vn = vctr < (uint32_t)prm.vst ? vctr : (uint32_t)prm.vst;
-      for (uint32_t i = vctr - vn; i < vctr; ++i) mbar_wait_drain(&bars->v_full[i % prm.vst], (i / prm.vst) & 1, limit);
+      // drain: every copy this thread issued lands before the CTA exits
+      if (is_k) {
+        mbar_wait_drain(&bars->q_full, 0, limit);
+        const uint32_t kn = ctr < (uint32_t)prm.kst ? ctr : (uint32_t)prm.kst;
+        for (uint32_t i = ctr - kn; i < ctr; ++i) mbar_wait_drain(&bars->k_full[i % prm.kst], (i / prm.kst) & 1, limit);
+      } else {
+        const uint32_t vn = ctr < (uint32_t)prm.vst ? ctr : (uint32_t)prm.vst;
+        for (uint32_t i = ctr - vn; i < ctr; ++i) mbar_wait_drain(&bars->v_full[i % prm.vst], (i / prm.vst) & 1, limit);
+      }
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
@@ -183,22 +209,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
       const uint32_t sq_addr = smem_u32(sq), sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
       bool ok = mbar_wait(&bars->q_full, 0, abortf, limit);
-      // S_t,blk = Q_t K_blk^T; K chunks of block blk sit in ring slots (blk*NC + c) % kst
+      // S_t,blk = Q_t K_blk^T.  K block blk sits in ring slot blk % kst; Q tile t
+      // chunk c at sq + c*32 KB + t*16 KB (one 256-row copy per chunk).
       auto issue_s = [&](int t, int blk, bool wait_full, bool release) -> bool {
+        const int s = blk % prm.kst;
+        if (wait_full && !mbar_wait(&bars->k_full[s], (blk / prm.kst) & 1, abortf, limit)) return false;
+        if (wait_full) ATTN_TRACE_EV(12, blk);
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          const uint32_t idx = (uint32_t)(blk * NC + c);
-          const int s = idx % prm.kst;
-          if (wait_full && !mbar_wait(&bars->k_full[s], (idx / prm.kst) & 1, abortf, limit)) return false;
-          tc_fence_after();
-          const uint32_t qaddr = sq_addr + (t * NC + c) * CHUNK_BYTES;
-          const uint32_t kaddr = sk_addr + s * CHUNK_BYTES;
+          const uint32_t qaddr = sq_addr + c * 2 * CHUNK_BYTES + t * CHUNK_BYTES;
+          const uint32_t kaddr = sk_addr + (s * NC + c) * CHUNK_BYTES;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ss(tmem + 128 * t, smem_desc(qaddr + kk * 32, 16, 1024), smem_desc(kaddr + kk * 32, 16, 1024),
                    idesc_s, (c | kk) != 0);
-          if (release) mma_commit(&bars->k_empty[s]);
         }
+        if (release) mma_commit(&bars->k_empty[s]);
         mma_commit(&bars->s_full[t]);
         return true;
       };
@@ -207,12 +234,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ok && act(1, 0)) ok = issue_s(1, 0, !act(0, 0), true);
       for (int j = 0; j < nblk && ok; ++j) {
         const int vs = j % prm.vst;
+        ATTN_TRACE_EV(10, j);
         if (!mbar_wait(&bars->v_full[vs], (j / prm.vst) & 1, abortf, limit)) { ok = false; break; }
+        ATTN_TRACE_EV(11, j);
         const uint32_t vaddr = sv_addr + vs * NC * CHUNK_BYTES;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!act(t, j)) continue;
           if (!mbar_wait(&bars->p_full[t], j & 1, abortf, limit)) { ok = false; break; }
+          ATTN_TRACE_EV(8 + t, j);
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
@@ -224,6 +254,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool last = (t == 1) || !act(1, j + 1);
             if (!issue_s(t, j + 1, first, last)) { ok = false; break; }
           }
+          if (t == 0) ATTN_TRACE_EV(15, j);
         }
         if (!ok) break;
         mma_commit(&bars->v_empty[vs]);
@@ -247,13 +278,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
 
+    const bool tr = (tid & 127) == 0;
     for (int j = 0; j < nb; ++j) {
+      if (tr) ATTN_TRACE_EV(4 * t + 0, j);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abortf, limit))) { ok = false; break; }
+      if (tr) ATTN_TRACE_EV(4 * t + 1, j);
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
       tmem_wait_ld();
+      if (tr) ATTN_TRACE_EV(4 * t + 2, j);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
       float x[BN];
@@ -332,6 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);
+      if (tr) ATTN_TRACE_EV(4 * t + 3, j);
     }
     if (!ok) raise_abort(bars, p.status);
 
@@ -388,11 +424,22 @@ template <int D>
 cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
   constexpr int NC = D / 64;
   const int avail = kSmemMax - 2048;
-  const int qb = 2 * NC * CHUNK_BYTES, vb = NC * CHUNK_BYTES;
-  int vst = 2;
-  int kst = (avail - qb - vst * vb) / CHUNK_BYTES;
+  const int qb = 2 * NC * CHUNK_BYTES, blkb = NC * CHUNK_BYTES;
+  // K and V rings in whole blocks; at least two of each, the rest to K
+  int vst = 2, kst = (avail - qb - vst * blkb) / blkb;
   if (kst > MAX_KST) kst = MAX_KST;
-  if (kst < NC) return cudaErrorInvalidConfiguration;
+  if (kst > 2 && vst < MAX_VST && kst > vst + 1) {
+    const int spare = kst - (vst + 1);
+    vst += spare / 2 < MAX_VST - vst ? spare / 2 : MAX_VST - vst;
+    kst = (avail - qb - vst * blkb) / blkb;
+    if (kst > MAX_KST) kst = MAX_KST;
+  }
+#ifdef ATTN_TC2_VST
+  vst = ATTN_TC2_VST;
+  kst = (avail - qb - vst * blkb) / blkb;
+  if (kst > MAX_KST) kst = MAX_KST;
+#endif
+  if (kst < 2 || vst < 2) return cudaErrorInvalidConfiguration;
   Params2 prm;
   memset(&prm, 0, sizeof(prm));
   prm.p = p;
@@ -400,15 +447,15 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
   prm.kst = kst;
   prm.vst = vst;
   prm.off_k = qb;
-  prm.off_v = qb + kst * CHUNK_BYTES;
-  prm.off_bar = prm.off_v + vst * vb;
+  prm.off_v = qb + kst * blkb;
+  prm.off_bar = prm.off_v + vst * blkb;
   prm.wait_limit_ns = wait_limit_ns;
   const int smem = prm.off_bar + (int)sizeof(Bars2) + 1024;
   if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
-  if (!make_tile_map(&tq, p.q, D, p.Nq, p.B * p.Hq)) return cudaErrorInvalidValue;
-  if (!make_tile_map(&tk, p.k, D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
-  if (!make_tile_map(&tv, p.v, D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
+  if (!make_block_map(&tq, p.q, D, p.Nq, p.B * p.Hq, 2 * BM)) return cudaErrorInvalidValue;
+  if (!make_block_map(&tk, p.k, D, p.Nkv, p.B * p.Hkv, BN)) return cudaErrorInvalidValue;
+  if (!make_block_map(&tv, p.v, D, p.Nkv, p.B * p.Hkv, BN)) return cudaErrorInvalidValue;
   static std::atomic<int> attr_set[64];
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[device].load(std::memory_order_acquire)) {
