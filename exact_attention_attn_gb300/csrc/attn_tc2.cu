@@ -34,18 +34,22 @@
 #include "attn_internal.h"
 #include "sm100_ptx.cuh"
 
-// Optional per-role timestamps (clock64) for a few CTAs, compiled in only
-// when ATTN_TRACE is defined: ATTN_TRACE_EV(row, col) stores into the
-// caller-provided buffer attn_trace_buf[cta][16][64].
+// Optional per-role timestamps (clock64) for the first 8 CTAs, compiled in
+// only when ATTN_TRACE is defined: ATTN_TRACE_EV(row, col) stores into the
+// caller-provided buffer attn_trace_buf[cta][24][64] (pointer read once per
+// thread by ATTN_TRACE_SETUP).
 #ifdef ATTN_TRACE
 __device__ long long *attn_trace_buf;
-#define ATTN_TRACE_EV(row, col)                                                                         \
-  do {                                                                                                  \
-    const long long _t = clock64();                                                                     \
-    long long *_b = attn_trace_buf;                                                                     \
-    if (_b && blockIdx.x < 8 && (col) < 64) _b[((long long)blockIdx.x * 16 + (row)) * 64 + (col)] = _t; \
+#define ATTN_TRACE_SETUP long long *const attn_tbuf = (blockIdx.x < 8) ? attn_trace_buf : nullptr
+#define ATTN_TRACE_EV(row, col)                                                              \
+  do {                                                                                       \
+    const long long _t = clock64();                                                          \
+    if (attn_tbuf && (col) < 64) attn_tbuf[((long long)blockIdx.x * 24 + (row)) * 64 + (col)] = _t; \
   } while (0)
 #else
+#define ATTN_TRACE_SETUP \
+  do {                   \
+  } while (0)
 #define ATTN_TRACE_EV(row, col) \
   do {                          \
   } while (0)
@@ -58,13 +62,26 @@ using namespace ptx;
 
 constexpr int BM = 128, BN = 128;
 constexpr int CHUNK_BYTES = 128 * 128;
+#ifdef ATTN_TRACE
+constexpr int THREADS = 384;  // + a trace-only observer warp
+#else
 constexpr int THREADS = 352;
+#endif
 constexpr int WARP_LOAD_K = 8, WARP_LOAD_V = 10, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float TAU = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int MAX_KST = 8, MAX_VST = 3;
+#ifndef ATTN_TC2_PREFETCH
+#define ATTN_TC2_PREFETCH 0
+#endif
+constexpr int kPrefetch = ATTN_TC2_PREFETCH;  // L2 prefetch distance in blocks
+// pairs q with bit (q % 8) set take the FMA-pipe exp2 (3 of 8)
+#ifndef ATTN_TC2_POLY_PAIRS
+#define ATTN_TC2_POLY_PAIRS 0x52
+#endif
+constexpr unsigned kPolyPairs = ATTN_TC2_POLY_PAIRS;
 constexpr int kSmemMax = 232448;
 
 struct Params2 {
@@ -111,11 +128,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   const Problem &p = prm.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t limit = prm.wait_limit_ns;
+  ATTN_TRACE_SETUP;
 
   // ---- work unit: (b, hq) fastest, then tile pair (heaviest causal pairs first)
   const int BH = p.B * p.Hq;
+#ifdef ATTN_TC2_HEAD_MAJOR
+  const int bh = blockIdx.x / prm.npairs;
+  const int t_idx = blockIdx.x % prm.npairs;
+#else
   const int bh = blockIdx.x % BH;
   const int t_idx = blockIdx.x / BH;
+#endif
   const int pair = p.causal ? (prm.npairs - 1 - t_idx) : t_idx;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
@@ -172,7 +195,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // both query tiles (256 rows, zero-filled past Nq) in one copy
         mbar_arrive_expect_tx(&bars->q_full, 2 * NC * CHUNK_BYTES);
         tma_load_4d(sq, &tm_q, &bars->q_full, 0, pair * 2 * BM, 0, bh);
+        // warm L2 with the first blocks; later ones are prefetched kPrefetch
+        // blocks ahead of their shared-memory copy
+        for (int j = 0; j < kPrefetch && j < nblk; ++j) tma_prefetch_4d(&tm_k, 0, j * BN, 0, bkv);
         for (int j = 0; j < nblk; ++j) {
+          if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_k, 0, (j + kPrefetch) * BN, 0, bkv);
           const int s = ctr % prm.kst;
           if (!mbar_wait(&bars->k_empty[s], ((ctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars->k_full[s], NC * CHUNK_BYTES);
@@ -182,7 +209,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
         tma_prefetch_desc(&tm_v);
+        for (int j = 0; j < kPrefetch && j < nblk; ++j) tma_prefetch_4d(&tm_v, 0, j * BN, 0, bkv);
         for (int j = 0; j < nblk; ++j) {
+          if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_v, 0, (j + kPrefetch) * BN, 0, bkv);
           const int vs = ctr % prm.vst;
           if (!mbar_wait(&bars->v_empty[vs], ((ctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars->v_full[vs], NC * CHUNK_BYTES);
@@ -216,14 +245,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (wait_full && !mbar_wait(&bars->k_full[s], (blk / prm.kst) & 1, abortf, limit)) return false;
         if (wait_full) ATTN_TRACE_EV(12, blk);
         tc_fence_after();
+        // descriptor of a K-major 128B-swizzled chunk; the K=16 step inside a
+        // chunk advances its start address by 32 bytes (2 in the >>4 field)
+        const uint64_t qd0 = smem_desc(sq_addr + t * CHUNK_BYTES, 16, 1024);
+        const uint64_t kd0 = smem_desc(sk_addr + s * NC * CHUNK_BYTES, 16, 1024);
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          const uint32_t qaddr = sq_addr + c * 2 * CHUNK_BYTES + t * CHUNK_BYTES;
-          const uint32_t kaddr = sk_addr + (s * NC + c) * CHUNK_BYTES;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + 128 * t, smem_desc(qaddr + kk * 32, 16, 1024), smem_desc(kaddr + kk * 32, 16, 1024),
-                   idesc_s, (c | kk) != 0);
+            mma_ss(tmem + 128 * t, qd0 + (uint64_t)(c * (2 * CHUNK_BYTES >> 4) + kk * 2),
+                   kd0 + (uint64_t)(c * (CHUNK_BYTES >> 4) + kk * 2), idesc_s, (c | kk) != 0);
         }
         if (release) mma_commit(&bars->k_empty[s]);
         mma_commit(&bars->s_full[t]);
@@ -244,10 +275,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!mbar_wait(&bars->p_full[t], j & 1, abortf, limit)) { ok = false; break; }
           ATTN_TRACE_EV(8 + t, j);
           tc_fence_after();
+          const uint64_t vd0 = smem_desc(vaddr, CHUNK_BYTES, 1024);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, smem_desc(vaddr + kk * 2048, CHUNK_BYTES, 1024),
-                   idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, vd0 + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
           if (j == nblk_t[t] - 1) mma_commit(&bars->o_done[t]);
           if (act(t, j + 1)) {
             const bool first = (t == 0) || !act(0, j + 1);
@@ -263,7 +295,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       mma_commit(&bars->done);
       if (!mbar_wait_drain(&bars->done, 0, limit)) raise_abort(bars, p.status);
     }
-  } else {
+#ifdef ATTN_TRACE
+  } else if (warp == 11) {
+    // trace-only observer: records when each K and V block lands
+    if (lane == 0 && nblk > 0) {
+      for (int j = 0; j < nblk; ++j) {
+        if (!mbar_wait(&bars->k_full[j % prm.kst], (j / prm.kst) & 1, abortf, limit)) break;
+        ATTN_TRACE_EV(16, j);
+        if (!mbar_wait(&bars->v_full[j % prm.vst], (j / prm.vst) & 1, abortf, limit)) break;
+        ATTN_TRACE_EV(17, j);
+      }
+    }
+#endif
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
     const int t = warp >> 2;          // tile of this warpgroup
     const int row = tid & 127;
@@ -277,6 +321,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool pos = sl2 > 0.f;  // uniform across the CTA
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
+    const Exp2Poly exp2_poly;
 
     const bool tr = (tid & 127) == 0;
     for (int j = 0; j < nb; ++j) {
@@ -296,32 +341,35 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
       const int kbase = j * BN;
-      if (kbase + BN > vis_end) {
+      const bool full = kbase + BN <= vis_end;  // no masked key in this block for this row
+      if (!full) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (kbase + c >= vis_end) x[c] = pos ? -INFINITY : INFINITY;
       }
-      // block max of the scaled scores, four independent chains
-      float mx[4];
+      // block max (min when scale < 0) of the raw scores, four chains of 3-input ops
+      float mblk;
       if (pos) {
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) mx[k4] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < BN; c += 4)
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) mx[k4] = fmaxf(mx[k4], x[c + k4]);
+        for (int c = 0; c < BN; c += 8) {
+          mx0 = max3f(mx0, x[c + 0], x[c + 1]);
+          mx1 = max3f(mx1, x[c + 2], x[c + 3]);
+          mx2 = max3f(mx2, x[c + 4], x[c + 5]);
+          mx3 = max3f(mx3, x[c + 6], x[c + 7]);
+        }
+        const float ext = max3f(mx0, mx1, fmaxf(mx2, mx3));
+        mblk = (ext == -INFINITY) ? -INFINITY : ext * sl2;
       } else {
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) mx[k4] = INFINITY;
+        float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
 #pragma unroll
         for (int c = 0; c < BN; c += 4)
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) mx[k4] = fminf(mx[k4], x[c + k4]);
+          for (int k4 = 0; k4 < 4; ++k4) mn[k4] = fminf(mn[k4], x[c + k4]);
+        const float ext = fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3]));
+        // ext*sl2 is the block max of the scaled scores; masked-only rows give -inf
+        mblk = (ext == INFINITY) ? -INFINITY : (sl2 == 0.f ? 0.f : ext * sl2);
       }
-      const float ext = pos ? fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]))
-                            : fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3]));
-      // ext*sl2 is the block max of the scaled scores; masked-only rows give -inf
-      const float mblk = (ext == (pos ? -INFINITY : INFINITY)) ? -INFINITY : (sl2 == 0.f ? 0.f : ext * sl2);
       const float m_new = fmaxf(m_use, mblk);
       if (__any_sync(0xffffffffu, m_new > m_use + TAU)) {
         const float alpha = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m_new);
@@ -342,28 +390,67 @@ __global__ void __launch_bounds__(THREADS, 1)
         m_use = m_new;
       }
       const float mu = (m_use == -INFINITY) ? 0.f : m_use;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // the branch must be warp-uniform: both sides end in the warp-collective
+      // tcgen05.st, which every lane of the warp has to execute together
+      if (__all_sync(0xffffffffu, pos && full)) {
+        // every key visible and scale > 0: y = s*sl2 - mu on f32x2 pairs;
+        // 3 of every 8 pairs take exp2 on the FMA pipe, the rest on the MUFU,
+        // so that neither unit alone bounds the block
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nmu2 = f2_pack(-mu, -mu);
+        uint64_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t pk[16];
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = x[h * 32 + 2 * i], bb = x[h * 32 + 2 * i + 1];
-          // masked entries hold -inf (or +inf when scale < 0) and give exactly 0
-          float p0, p1;
-          if (pos) {
-            p0 = ex2_approx(fmaf(a, sl2, -mu));
-            p1 = ex2_approx(fmaf(bb, sl2, -mu));
-          } else {
-            p0 = (a == INFINITY) ? 0.f : ex2_approx(fmaf(a, sl2, -mu));
-            p1 = (bb == INFINITY) ? 0.f : ex2_approx(fmaf(bb, sl2, -mu));
+          for (int i = 0; i < 16; ++i) {
+            const int q = h * 16 + i;
+            const uint64_t y = f2_fma(f2_pack(x[2 * q], x[2 * q + 1]), sl2x2, nmu2);
+            uint64_t p2;
+            if ((kPolyPairs >> (q & 7)) & 1) {
+              p2 = exp2_poly(y);
+            } else {
+              float y0, y1;
+              f2_unpack(y, y0, y1);
+              p2 = f2_pack(ex2_approx(y0), ex2_approx(y1));
+            }
+            if (i & 1)
+              acc1 = f2_add(acc1, p2);
+            else
+              acc0 = f2_add(acc0, p2);
+            float p0, p1;
+            f2_unpack(p2, p0, p1);
+            pk[i] = pack_bf16x2(p0, p1);
           }
-          ls[i & 3] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          tmem_st16(tS + h * 16, pk);
         }
-        tmem_st16(tS + h * 16, pk);
+        float a0, a1, b0, b1;
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, b0, b1);
+        l += (a0 + a1) + (b0 + b1);
+      } else {
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = x[h * 32 + 2 * i], bb = x[h * 32 + 2 * i + 1];
+            // masked entries hold -inf (or +inf when scale < 0) and give exactly 0
+            float p0, p1;
+            if (pos) {
+              p0 = ex2_approx(fmaf(a, sl2, -mu));
+              p1 = ex2_approx(fmaf(bb, sl2, -mu));
+            } else {
+              p0 = (a == INFINITY) ? 0.f : ex2_approx(fmaf(a, sl2, -mu));
+              p1 = (bb == INFINITY) ? 0.f : ex2_approx(fmaf(bb, sl2, -mu));
+            }
+            ls[i & 3] += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + h * 16, pk);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);

@@ -104,6 +104,14 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *m
       : "memory");
 }
 
+// Prefetch a 4-D tile into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // Allocate `ncols` TMEM columns (power of two >= 32); the TMEM address is
@@ -218,6 +226,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// Per-warp register budget change (whole warp; the warpgroup's four warps
+// must agree).  The block's pool is its launch allocation, so the budgets of
+// all warps must add up to at most threads x registers-at-launch.
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
@@ -252,6 +272,71 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// ---- packed fp32 pairs (f32x2 arithmetic of the sm_100 family)
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^y for a pair of floats on the FMA pipe (no MUFU): Cody-Waite range
+// reduction y = j + f, j = round-to-nearest(y) (the 1.5*2^23 addition trick),
+// f in [-1/2, 1/2]; 2^f by a degree-3 polynomial minimising the relative error
+// on that interval (Remez exchange, coefficients from csrc/fit_exp2_poly.py,
+// max relative error 7.5e-5); 2^j applied by adding j to the exponent field.
+// y is clamped at -126, so very negative inputs (and -inf) give about 2^-126
+// instead of 0: callers use it only where every input is finite and the
+// result is summed against values of order 1.
+struct Exp2Poly {
+  uint64_t magic, neg_magic, neg_one, c0, c1, c2, c3;
+  __device__ __forceinline__ Exp2Poly() {
+    magic = f2_pack(12582912.0f, 12582912.0f);
+    neg_magic = f2_pack(-12582912.0f, -12582912.0f);
+    neg_one = f2_pack(-1.0f, -1.0f);
+    c0 = f2_pack(0.9999280571937561f, 0.9999280571937561f);
+    c1 = f2_pack(0.6932609677314758f, 0.6932609677314758f);
+    c2 = f2_pack(0.2426111251115799f, 0.2426111251115799f);
+    c3 = f2_pack(0.0551716685295105f, 0.0551716685295105f);
+  }
+  __device__ __forceinline__ uint64_t operator()(uint64_t y) const {
+    float y0, y1;
+    f2_unpack(y, y0, y1);
+    const uint64_t yc = f2_pack(fmaxf(y0, -126.f), fmaxf(y1, -126.f));
+    const uint64_t t = f2_add(yc, magic);         // 1.5*2^23 + j in the mantissa
+    const uint64_t jf = f2_add(t, neg_magic);     // j
+    const uint64_t fr = f2_fma(jf, neg_one, yc);  // f = y - j
+    uint64_t pp = f2_fma(c3, fr, c2);
+    pp = f2_fma(pp, fr, c1);
+    pp = f2_fma(pp, fr, c0);
+    float p0, p1, t0, t1;
+    f2_unpack(pp, p0, p1);
+    f2_unpack(t, t0, t1);
+    // the low bits of t hold j; (t << 23) adds j to the exponent field
+    const uint32_t r0 = __float_as_uint(p0) + (__float_as_uint(t0) << 23);
+    const uint32_t r1 = __float_as_uint(p1) + (__float_as_uint(t1) << 23);
+    return f2_pack(__uint_as_float(r0), __uint_as_float(r1));
+  }
+};
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
