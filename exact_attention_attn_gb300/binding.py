@@ -57,6 +57,8 @@ def load_library() -> ctypes.CDLL:
         vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd.restype = ci
+        lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+        lib.attn_fwd_splitkv.restype = ci
         lib.attn_fwd_status.argtypes = [vp]
         lib.attn_fwd_status.restype = ci
         lib.attn_strerror.argtypes = [ci]
@@ -102,11 +104,13 @@ def _check(t: torch.Tensor, name: str, dtype, ndim: int):
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
              causal: bool = False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-             stream=None):
+             stream=None, kv_splits: int | None = None):
     """O, LSE = attention forward of bf16 q [B,Hq,Nq,D], k and v [B,Hkv,Nkv,D].
 
     O is bf16 [B,Hq,Nq,D]; LSE is fp32 [B,Hq,Nq] (natural log).  Runs
     asynchronously on ``stream`` (default: torch's current stream).
+    ``kv_splits`` (None/0 = automatic) forces the number of key-range splits
+    (attn_fwd_splitkv).
     """
     lib = load_library()
     _check(q, "q", torch.bfloat16, 4)
@@ -127,8 +131,13 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | N
     if tuple(out.shape) != (B, Hq, Nq, D) or tuple(lse.shape) != (B, Hq, Nq):
         raise ValueError("out / lse shape mismatch")
     with torch.cuda.device(q.device):
-        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                          B, Hq, Hkv, Nq, Nkv, D, float(scale), int(bool(causal)), _stream_handle(stream))
+        if kv_splits:
+            rc = lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                      B, Hq, Hkv, Nq, Nkv, D, float(scale), int(bool(causal)), int(kv_splits),
+                                      _stream_handle(stream))
+        else:
+            rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              B, Hq, Hkv, Nq, Nkv, D, float(scale), int(bool(causal)), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return out, lse

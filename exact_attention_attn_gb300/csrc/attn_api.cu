@@ -79,34 +79,102 @@ int check_sizes(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal) {
   return ATTN_OK;
 }
 
-void make_plan(const Problem &p, const DeviceInfo &dev, attn_plan *plan) {
-  (void)dev;
+constexpr int kMaxSplits = 64;
+
+// CTAs of the tensor-core launch for one key range per query tile.
+int64_t base_ctas(const Problem &p) {
+  const int64_t tiles = (p.Nq + 127) / 128;
+  if (tc2_supports(p.D)) return ((tiles + 1) / 2) * p.B * p.Hq;
+  return tiles * p.B * p.Hq * tc_config(p.D).nslices;
+}
+
+// Key-range splits when one CTA per query tile leaves SMs idle: the split
+// count s (<= 16, at least two key blocks per range, at most two waves of
+// CTAs so that the fp32 partials stay small next to the work) that minimises
+// the number of CTA waves per unit of work, ceil(ctas*s / SMs) / s; kept at 1
+// unless that saves at least 10 %.
+int auto_splits(const Problem &p, int sm_count) {
+  const int64_t ctas = base_ctas(p);
+  const int64_t kblocks = (p.Nkv + 127) / 128;
+  if (ctas >= sm_count || kblocks < 4) return 1;
+  const int64_t smax = (2 * (int64_t)sm_count) / ctas;
+  int best = 1;
+  double best_cost = 1.0;
+  for (int s = 2; s <= 16 && s <= smax && kblocks / s >= 2; ++s) {
+    const double cost = (double)((ctas * s + sm_count - 1) / sm_count) / s;
+    if (cost < best_cost * 0.9 - 1e-12 || (cost < best_cost - 1e-12 && best > 1)) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// splits: 0 = choose automatically, otherwise the caller's count.
+void make_plan(const Problem &p, const DeviceInfo &dev, int splits, attn_plan *plan) {
   memset(plan, 0, sizeof(*plan));
+  plan->kv_splits = 1;
+  plan->d_slices = 1;
   if (p.B == 0 || p.Nq == 0) {
     plan->path = ATTN_PATH_NONE;
-    plan->kv_splits = 1;
-    plan->d_slices = 1;
     return;
   }
   if (p.Nkv == 0) {  // no keys: every row is O = 0, LSE = -inf
     plan->path = ATTN_PATH_SIMT;
     plan->launches = 1;
-    plan->kv_splits = 1;
     plan->d_slices = (p.D + 255) / 256;
     plan->grid = (int)(((int64_t)(p.Nq + 63) / 64) * p.B * p.Hq * plan->d_slices);
     return;
   }
-  plan->path = ATTN_PATH_TC;
-  plan->launches = 1;
-  plan->kv_splits = 1;
-  if (tc2_supports(p.D)) {
-    plan->d_slices = 1;
-    plan->grid = (int)((((int64_t)(p.Nq + 127) / 128 + 1) / 2) * p.B * p.Hq);
+  const int s = splits > 0 ? splits : auto_splits(p, dev.sm_count);
+  plan->kv_splits = s;
+  plan->d_slices = tc2_supports(p.D) ? 1 : tc_config(p.D).nslices;
+  plan->grid = (int)(base_ctas(p) * s);
+  if (s == 1) {
+    plan->path = ATTN_PATH_TC;
+    plan->launches = 1;
   } else {
-    const TcConfig c = tc_config(p.D);
-    plan->d_slices = c.nslices;
-    plan->grid = (int)(((int64_t)(p.Nq + 127) / 128) * p.B * p.Hq * c.nslices);
+    plan->path = ATTN_PATH_TC_SPLITKV;
+    plan->launches = 2;
+    plan->workspace_bytes = (long long)s * p.B * p.Hq * (long long)p.Nq * (p.D + 1) * 4;
   }
+}
+
+int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  switch (plan.path) {
+    case ATTN_PATH_NONE:
+      return ATTN_OK;
+    case ATTN_PATH_SIMT:
+      p.kv_splits = 1;
+      e = launch_simt(p, st);
+      break;
+    case ATTN_PATH_TC:
+      p.kv_splits = 1;
+      e = tc2_supports(p.D) ? launch_tc2(p, dev.device, kWaitLimitNs, st) : launch_tc(p, dev.device, kWaitLimitNs, st);
+      break;
+    case ATTN_PATH_TC_SPLITKV: {
+      // stream-ordered workspace: allocated and freed on the caller's stream
+      void *ws = nullptr;
+      if (cudaMallocAsync(&ws, (size_t)plan.workspace_bytes, st) != cudaSuccess || !ws) {
+        cudaGetLastError();
+        return ATTN_ERR_NOMEM;
+      }
+      const int64_t rows = (int64_t)p.B * p.Hq * p.Nq;
+      p.kv_splits = plan.kv_splits;
+      p.ws_o = static_cast<float *>(ws);
+      p.ws_lse = p.ws_o + (int64_t)plan.kv_splits * rows * p.D;
+      e = tc2_supports(p.D) ? launch_tc2(p, dev.device, kWaitLimitNs, st) : launch_tc(p, dev.device, kWaitLimitNs, st);
+      if (e == cudaSuccess) e = launch_combine(p, st);
+      cudaError_t f = cudaFreeAsync(ws, st);
+      if (e == cudaSuccess) e = f;
+      break;
+    }
+    default:
+      return ATTN_ERR_ARG;
+  }
+  if (e != cudaSuccess) return record(e);
+  return ATTN_OK;
 }
 
 }  // namespace
@@ -132,13 +200,13 @@ const char *attn_strerror(int code) {
 
 const char *attn_last_cuda_error(void) { return attn::t_last_error; }
 
-int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
-             int B, int Hq, int Hkv, int Nq, int Nkv, int D,
-             float scale, int causal, attn_stream_t stream) {
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                     float scale, int causal, int kv_splits, attn_stream_t stream) {
   using namespace attn;
   int rc = check_sizes(B, Hq, Hkv, Nq, Nkv, D, causal);
   if (rc != ATTN_OK) return rc;
-  if (!isfinite(scale)) return ATTN_ERR_ARG;
+  if (!isfinite(scale) || kv_splits < 0 || kv_splits > kMaxSplits) return ATTN_ERR_ARG;
   if (B == 0 || Nq == 0) return ATTN_OK;
   if (!q || !o || !lse) return ATTN_ERR_ARG;
   if (Nkv > 0 && (!k || !v)) return ATTN_ERR_ARG;
@@ -149,7 +217,7 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
   rc = device_info(&dev);
   if (rc != ATTN_OK) return rc;
 
-  Problem p;
+  Problem p{};
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.k = static_cast<const __nv_bfloat16 *>(k);
   p.v = static_cast<const __nv_bfloat16 *>(v);
@@ -159,20 +227,17 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
   p.scale = scale;
   p.causal = causal;
   p.status = dev->status;
+  p.kv_splits = 1;
 
   attn_plan plan;
-  make_plan(p, *dev, &plan);
-  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaSuccess;
-  switch (plan.path) {
-    case ATTN_PATH_SIMT: e = launch_simt(p, st); break;
-    case ATTN_PATH_TC:
-      e = tc2_supports(p.D) ? launch_tc2(p, dev->device, kWaitLimitNs, st) : launch_tc(p, dev->device, kWaitLimitNs, st);
-      break;
-    default: return ATTN_OK;
-  }
-  if (e != cudaSuccess) return record(e);
-  return ATTN_OK;
+  make_plan(p, *dev, kv_splits, &plan);
+  return launch_plan(p, *dev, plan, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+             float scale, int causal, attn_stream_t stream) {
+  return attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal, 0, stream);
 }
 
 int attn_fwd_plan(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, attn_plan *plan) {
@@ -185,7 +250,7 @@ int attn_fwd_plan(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal, at
   if (rc != ATTN_OK) return rc;
   Problem p{};
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.Nkv = Nkv; p.D = D; p.causal = causal;
-  make_plan(p, *dev, plan);
+  make_plan(p, *dev, 0, plan);
   return ATTN_OK;
 }
 

@@ -20,6 +20,13 @@ struct Problem {
   float scale;
   int causal;
   int *status;             // device status word (first error wins)
+  // split-KV: kv_splits CTAs share each query tile, each over a contiguous
+  // range of key blocks; with kv_splits > 1 the kernels write normalised fp32
+  // partial outputs ws_o [kv_splits, B*Hq, Nq, D] and partial natural-log
+  // LSEs ws_lse [kv_splits, B*Hq, Nq] instead of o and lse.
+  int kv_splits;
+  float *ws_o;
+  float *ws_lse;
 };
 
 // Device status codes written by kernels (same values as the public ATTN_ERR_*).
@@ -56,6 +63,10 @@ cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cuda
 // Two-tile ping-pong tensor-core kernel for head dims 64 and 128.
 bool tc2_supports(int D);
 cudaError_t launch_tc2(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream);
+
+// Merge kv_splits partial results into o (bf16) and lse: LSE = ln sum_s
+// exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.  Memory-bound, one pass.
+cudaError_t launch_combine(const Problem &p, cudaStream_t stream);
 
 // Plain CUDA-core kernel: correct for every supported shape; used for the
 // shapes the tensor-core kernel does not take.

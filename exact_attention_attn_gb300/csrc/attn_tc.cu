@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- work unit: output slice fastest, then (b, hq), then query tile
   //      (heaviest causal tiles first)
   int bid = blockIdx.x;
+  const int nsplit = p.kv_splits;
+  const int split = bid % nsplit;
+  bid /= nsplit;
   const int slice = bid % prm.nslices;
   bid /= prm.nslices;
   const int BH = p.B * p.Hq;
@@ -126,7 +129,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int shift = p.Nkv - p.Nq;  // bottom-right causal alignment
   int kv_end = p.Nkv;
   if (p.causal) kv_end = max(0, min(p.Nkv, q0 + BM - 1 + shift + 1));
-  const int nblk = (kv_end + BN - 1) / BN;
+  // this CTA's key blocks: [jb, jb + nblk) of the tile's range, split evenly;
+  // block indices j below are relative to jb
+  const int nall = (kv_end + BN - 1) / BN;
+  const int jb = (int)((int64_t)split * nall / nsplit);
+  const int nblk = (int)((int64_t)(split + 1) * nall / nsplit) - jb;
 
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int s = kctr % prm.kst;
           if (!mbar_wait(&bars->k_empty[s], ((kctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars->k_full[s], CHUNK_BYTES);
-          tma_load_3d(sk + s * CHUNK_BYTES, &tm_k, &bars->k_full[s], c * 64, j * BN, bkv);
+          tma_load_3d(sk + s * CHUNK_BYTES, &tm_k, &bars->k_full[s], c * 64, (jb + j) * BN, bkv);
           ++kctr;
         }
         if (!ok) break;
@@ -190,7 +197,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(&bars->v_full[vs], s_chunks * CHUNK_BYTES);
         uint8_t *vdst = sv + vs * (prm.vmax * CHUNK_BYTES);
         for (int c = 0; c < s_chunks; ++c)
-          tma_load_3d(vdst + c * CHUNK_BYTES, &tm_v, &bars->v_full[vs], (s_c0 + c) * 64, j * BN, bkv);
+          tma_load_3d(vdst + c * CHUNK_BYTES, &tm_v, &bars->v_full[vs], (s_c0 + c) * 64, (jb + j) * BN, bkv);
         ++vctr;
       }
       if (!ok) raise_abort(bars, p.status);
@@ -292,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(&bars->s_free);
 
       // scale to log2 units, mask, block max
-      const int kbase = j * BN;
+      const int kbase = (jb + j) * BN;
       float mblk = -INFINITY;
       if (kbase + BN <= vis_end) {
 #pragma unroll
@@ -367,6 +374,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok) {
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const float lse_val = (m_use == -INFINITY || !(l > 0.f)) ? -INFINITY : (m_use + log2f(l)) * kLn2;
+      const int64_t row_idx = (int64_t)bh * p.Nq + qi;
+      // split-KV: normalised fp32 partial O_s and LSE_s of this key range
+      float *wrow = (nsplit > 1) ? p.ws_o + ((int64_t)split * BH * p.Nq + row_idx) * p.D + s_c0 * 64 : nullptr;
       for (int cc = 0; cc < DV / 32; ++cc) {
         uint32_t r[32];
         if (nblk > 0) {
@@ -378,20 +389,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
         if (qi < p.Nq) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+          if (nsplit == 1) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
-            dst[v4] = w;
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
+              dst[v4] = w;
+            }
+          } else {
+            float4 *dst = reinterpret_cast<float4 *>(wrow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(r[v4 * 4 + 0]) * inv, __uint_as_float(r[v4 * 4 + 1]) * inv,
+                                    __uint_as_float(r[v4 * 4 + 2]) * inv, __uint_as_float(r[v4 * 4 + 3]) * inv);
           }
         }
       }
-      if (slice == 0 && qi < p.Nq)
-        p.lse[(int64_t)bh * p.Nq + qi] = (m_use == -INFINITY || !(l > 0.f)) ? -INFINITY : (m_use + log2f(l)) * kLn2;
+      if (slice == 0 && qi < p.Nq) {
+        if (nsplit == 1)
+          p.lse[row_idx] = lse_val;
+        else
+          p.ws_lse[(int64_t)split * BH * p.Nq + row_idx] = lse_val;
+      }
     }
   }
 
@@ -459,7 +482,7 @@ cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cuda
   prm.off_v = c.off_v;
   prm.off_bar = c.off_bar;
   prm.wait_limit_ns = wait_limit_ns;
-  const int64_t grid = (int64_t)prm.ntiles * p.B * p.Hq * c.nslices;
+  const int64_t grid = (int64_t)prm.ntiles * p.B * p.Hq * c.nslices * p.kv_splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   // the opt-in shared-memory limit is a per-device function attribute: raise
   // it to the maximum once per device

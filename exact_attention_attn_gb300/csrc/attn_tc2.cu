@@ -132,12 +132,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   // ---- work unit: (b, hq) fastest, then tile pair (heaviest causal pairs first)
   const int BH = p.B * p.Hq;
+  const int nsplit = p.kv_splits;
+  const int split = blockIdx.x % nsplit;
+  const int unit = blockIdx.x / nsplit;
 #ifdef ATTN_TC2_HEAD_MAJOR
-  const int bh = blockIdx.x / prm.npairs;
-  const int t_idx = blockIdx.x % prm.npairs;
+  const int bh = unit / prm.npairs;
+  const int t_idx = unit % prm.npairs;
 #else
-  const int bh = blockIdx.x % BH;
-  const int t_idx = blockIdx.x / BH;
+  const int bh = unit % BH;
+  const int t_idx = unit / BH;
 #endif
   const int pair = p.causal ? (prm.npairs - 1 - t_idx) : t_idx;
   const int b = bh / p.Hq, hq = bh % p.Hq;
@@ -151,7 +154,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (p.causal) kv_end = max(0, min(p.Nkv, q0 + BM - 1 + shift + 1));
     nblk_t[t] = (q0 < p.Nq) ? (kv_end + BN - 1) / BN : 0;
   }
-  const int nblk = max(nblk_t[0], nblk_t[1]);
+  // this CTA's key blocks: [jb, jb + nblk) of the pair's range, split evenly;
+  // from here on nblk_t[t] counts the blocks tile t takes in that range and
+  // every block index j is relative to jb
+  const int nall = max(nblk_t[0], nblk_t[1]);
+  const int jb = (int)((int64_t)split * nall / nsplit);
+  const int je = (int)((int64_t)(split + 1) * nall / nsplit);
+#pragma unroll
+  for (int t = 0; t < 2; ++t) nblk_t[t] = max(0, min(je, nblk_t[t]) - jb);
+  const int nblk = je - jb;
 
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
@@ -197,25 +208,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_4d(sq, &tm_q, &bars->q_full, 0, pair * 2 * BM, 0, bh);
         // warm L2 with the first blocks; later ones are prefetched kPrefetch
         // blocks ahead of their shared-memory copy
-        for (int j = 0; j < kPrefetch && j < nblk; ++j) tma_prefetch_4d(&tm_k, 0, j * BN, 0, bkv);
+        for (int j = 0; j < kPrefetch && j < nblk; ++j) tma_prefetch_4d(&tm_k, 0, (jb + j) * BN, 0, bkv);
         for (int j = 0; j < nblk; ++j) {
-          if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_k, 0, (j + kPrefetch) * BN, 0, bkv);
+          if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_k, 0, (jb + j + kPrefetch) * BN, 0, bkv);
           const int s = ctr % prm.kst;
           if (!mbar_wait(&bars->k_empty[s], ((ctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars->k_full[s], NC * CHUNK_BYTES);
-          tma_load_4d(sk + s * NC * CHUNK_BYTES, &tm_k, &bars->k_full[s], 0, j * BN, 0, bkv);
+          tma_load_4d(sk + s * NC * CHUNK_BYTES, &tm_k, &bars->k_full[s], 0, (jb + j) * BN, 0, bkv);
           ATTN_TRACE_EV(13, j);
           ++ctr;
         }
       } else {
         tma_prefetch_desc(&tm_v);
-        for (int j = 0; j < kPrefetch && j < nblk; ++j) tma_prefetch_4d(&tm_v, 0, j * BN, 0, bkv);
+        for (int j = 0; j < kPrefetch && j < nblk; ++j) tma_prefetch_4d(&tm_v, 0, (jb + j) * BN, 0, bkv);
         for (int j = 0; j < nblk; ++j) {
-          if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_v, 0, (j + kPrefetch) * BN, 0, bkv);
+          if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_v, 0, (jb + j + kPrefetch) * BN, 0, bkv);
           const int vs = ctr % prm.vst;
           if (!mbar_wait(&bars->v_empty[vs], ((ctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars->v_full[vs], NC * CHUNK_BYTES);
-          tma_load_4d(sv + vs * NC * CHUNK_BYTES, &tm_v, &bars->v_full[vs], 0, j * BN, 0, bkv);
+          tma_load_4d(sv + vs * NC * CHUNK_BYTES, &tm_v, &bars->v_full[vs], 0, (jb + j) * BN, 0, bkv);
           ATTN_TRACE_EV(14, j);
           ++ctr;
         }
@@ -340,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
-      const int kbase = j * BN;
+      const int kbase = (jb + j) * BN;
       const bool full = kbase + BN <= vis_end;  // no masked key in this block for this row
       if (!full) {
 #pragma unroll
@@ -468,33 +479,60 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok) {
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16 *orow = p.o + ((int64_t)bh * p.Nq + qi) * D;
+      const float lse_val = (m_use == -INFINITY || !(l > 0.f)) ? -INFINITY : (m_use + log2f(l)) * kLn2;
+      const int64_t row_idx = (int64_t)bh * p.Nq + qi;
+      if (nsplit == 1) {
+        __nv_bfloat16 *orow = p.o + row_idx * D;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        if (nb > 0) {
-          tmem_ld32(tO + cc * 32, r);
-          tmem_wait_ld();
-          reg_fence32(r);
-        } else {
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          if (nb > 0) {
+            tmem_ld32(tO + cc * 32, r);
+            tmem_wait_ld();
+            reg_fence32(r);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
-        }
-        if (qi < p.Nq) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (qi < p.Nq) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
-            dst[v4] = w;
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
+              dst[v4] = w;
+            }
           }
         }
+        if (qi < p.Nq) p.lse[row_idx] = lse_val;
+      } else {
+        // partial result of this key range: O_s = acc / l_s (fp32), LSE_s
+        const int64_t ws_row = (int64_t)split * BH * p.Nq + row_idx;
+        float *orow = p.ws_o + ws_row * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          if (nb > 0) {
+            tmem_ld32(tO + cc * 32, r);
+            tmem_wait_ld();
+            reg_fence32(r);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (qi < p.Nq) {
+            float4 *dst = reinterpret_cast<float4 *>(orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(r[v4 * 4 + 0]) * inv, __uint_as_float(r[v4 * 4 + 1]) * inv,
+                                    __uint_as_float(r[v4 * 4 + 2]) * inv, __uint_as_float(r[v4 * 4 + 3]) * inv);
+          }
+        }
+        if (qi < p.Nq) p.ws_lse[ws_row] = lse_val;
       }
-      if (qi < p.Nq)
-        p.lse[(int64_t)bh * p.Nq + qi] = (m_use == -INFINITY || !(l > 0.f)) ? -INFINITY : (m_use + log2f(l)) * kLn2;
     }
   }
 
@@ -550,7 +588,7 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
     if (e != cudaSuccess) return e;
     attr_set[device].store(1, std::memory_order_release);
   }
-  const int64_t grid = (int64_t)prm.npairs * p.B * p.Hq;
+  const int64_t grid = (int64_t)prm.npairs * p.B * p.Hq * p.kv_splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   attn_tc2_kernel<D><<<(unsigned)grid, THREADS, smem, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError();

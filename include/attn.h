@@ -93,6 +93,28 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, floa
              float scale, int causal, attn_stream_t stream);
 
 /*
+ * attn_fwd_splitkv -- attn_fwd with an explicit number of key-range splits.
+ *
+ * The key blocks of every query tile are cut into kv_splits contiguous
+ * ranges, each handled by its own CTA, which writes a normalised fp32 partial
+ * output and a partial LSE; a second kernel merges them (LSE = ln sum_s
+ * exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s) -- the merge of partial results
+ * over key ranges through their LSE described on the ZYFA page ("The details
+ * that make it production-grade").  This spreads a problem with few query
+ * tiles and many keys over all SMs.
+ *
+ * kv_splits: 0 chooses automatically (what attn_fwd does); 1 disables the
+ *   split; 2..64 forces that many ranges (ranges left empty are harmless).
+ * Workspace: kv_splits * B * Hq * Nq * (D + 1) * 4 bytes, taken with
+ *   cudaMallocAsync on `stream` and released with cudaFreeAsync on the same
+ *   stream after the merge; ATTN_ERR_NOMEM if it cannot be had.
+ * Everything else (arguments, layouts, asynchrony, errors) is as attn_fwd.
+ */
+ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                              float scale, int causal, int kv_splits, attn_stream_t stream);
+
+/*
  * attn_fwd_status -- synchronise `stream`, then read and clear the device
  * status word of the current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a
  * bounded mbarrier wait inside a kernel gave up; that kernel's outputs are
@@ -110,7 +132,7 @@ ATTN_API const char *attn_last_cuda_error(void);
 
 /*
  * attn_fwd_plan -- describe, without launching anything, the kernels attn_fwd
- * would run for these sizes on the current device.  Sizes are checked as in
+ * (automatic split choice) would run for these sizes on the current device.  Sizes are checked as in
  * attn_fwd (pointers are not involved).  Fills *plan and returns ATTN_OK, or
  * returns a negative ATTN_ERR_* code.
  */

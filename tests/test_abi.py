@@ -32,7 +32,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_status", "attn_strerror", "attn_version"} <= names
+    assert {"attn_fwd", "attn_fwd_splitkv", "attn_fwd_plan", "attn_fwd_status", "attn_strerror", "attn_version"} <= names
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
@@ -85,6 +85,17 @@ def test_argument_errors(lib):
     # empty problems succeed without touching a device
     assert call(lib, None, None, None, None, None, B=0) == 0
     assert call(lib, None, None, None, None, None, Nq=0) == 0
+
+
+def test_splitkv_argument_errors(lib):
+    import ctypes as C
+    lib.attn_fwd_splitkv.argtypes = [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_float, C.c_int, C.c_int, C.c_void_p]
+    b = Buf()
+    p = b.p
+    assert lib.attn_fwd_splitkv(p, p, p, p, p, 1, 2, 1, 8, 8, 64, 0.125, 0, -1, None) == -1
+    assert lib.attn_fwd_splitkv(p, p, p, p, p, 1, 2, 1, 8, 8, 64, 0.125, 0, 65, None) == -1
+    assert lib.attn_fwd_splitkv(p, p, p, p, p, 1, 2, 1, 8, 8, 65, 0.125, 0, 2, None) == -1
+    assert lib.attn_fwd_splitkv(None, None, None, None, None, 0, 2, 1, 8, 8, 64, 0.125, 0, 2, None) == 0
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -103,3 +103,59 @@ def test_stream_argument():
     o2, _ = attn_fwd(q, k, v)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+# ---------------------------------------------------------------------------
+# split-KV: key ranges merged through their LSE
+
+SPLIT_CASES = [
+    (1, 2, 2, 200, 1000, 64, False),
+    (1, 2, 1, 300, 700, 128, True),
+    (2, 4, 2, 129, 1500, 128, False),
+    (1, 2, 2, 256, 300, 128, True),     # fewer key blocks than some split counts: empty ranges
+    (1, 1, 1, 100, 900, 192, False),
+    (1, 2, 2, 150, 600, 512, True),
+    (1, 1, 1, 128, 700, 1024, False),
+    (1, 2, 1, 300, 100, 128, True),     # causal, Nq > Nkv: fully masked rows in every range
+]
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=[str(c) for c in SPLIT_CASES])
+def test_splitkv_forced(case, splits):
+    B, Hq, Hkv, Nq, Nkv, D, causal = case
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nkv, D, seed=splits * 31 + D)
+    scale = 1.0 / np.sqrt(D)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    out = torch.full((B, Hq, Nq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, Hq, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    attn_fwd(dq, dk, dv, scale=scale, causal=causal, out=out, lse=lse, kv_splits=splits)
+    torch.cuda.synchronize()
+    mx, mean, dl = compare(out.cpu(), lse.cpu(), q, k, v, scale, causal)
+    assert mx <= 2e-2 and mean <= 2e-3 and dl <= 1e-3, (mx, mean, dl)
+
+
+def test_splitkv_auto_for_few_tiles():
+    from exact_attention_attn_gb300 import attn_fwd_plan
+    B, Hq, Hkv, Nq, Nkv, D = 1, 2, 1, 256, 16384, 128
+    plan = attn_fwd_plan(B, Hq, Hkv, Nq, Nkv, D, False)
+    assert plan["path_name"] == "tc_splitkv" and plan["kv_splits"] > 1 and plan["launches"] == 2
+    assert plan["workspace_bytes"] == plan["kv_splits"] * B * Hq * Nq * (D + 1) * 4
+    check_case(B, Hq, Hkv, Nq, Nkv, D, False, seed=77, nrows=64)
+
+
+def test_splitkv_deterministic():
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 2, 300, 2000, 128, 5))
+    o1, l1 = attn_fwd(q, k, v, causal=True, kv_splits=5)
+    o2, l2 = attn_fwd(q, k, v, causal=True, kv_splits=5)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_workload_plans():
+    from exact_attention_attn_gb300 import attn_fwd_plan
+    for name in WORKLOAD_ORDER:
+        w = WORKLOADS[name]
+        plan = attn_fwd_plan(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal)
+        assert plan["path_name"] in ("tc", "tc_splitkv"), (name, plan)
+        assert plan["grid"] > 0
