@@ -20,7 +20,7 @@ _lock = threading.Lock()
 
 ATTN_OK = 0
 _ERRORS = {-1: "ATTN_ERR_ARG", -2: "ATTN_ERR_ALIGN", -3: "ATTN_ERR_ARCH", -4: "ATTN_ERR_LAUNCH",
-           -5: "ATTN_ERR_TIMEOUT", -6: "ATTN_ERR_NOMEM", -7: "ATTN_ERR_DEVICE"}
+           -5: "ATTN_ERR_TIMEOUT", -6: "ATTN_ERR_NOMEM", -7: "ATTN_ERR_DEVICE", -8: "ATTN_ERR_SCRATCH"}
 
 
 class AttnPlan(ctypes.Structure):
@@ -59,6 +59,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd.restype = ci
         lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
         lib.attn_fwd_splitkv.restype = ci
+        lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+        lib.attn_fwd_splitkv_noalloc.restype = ci
         lib.attn_fwd_status.argtypes = [vp]
         lib.attn_fwd_status.restype = ci
         lib.attn_strerror.argtypes = [ci]

@@ -178,6 +178,21 @@ int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaSt
 }
 
 }  // namespace
+
+// For other translation units of the library: the current device's facts
+// (same per-device cache and checks as attn_fwd) and the last-error record.
+int current_device(int *device, int *sm_count, int **status) {
+  DeviceInfo *d = nullptr;
+  const int rc = device_info(&d);
+  if (rc != ATTN_OK) return rc;
+  *device = d->device;
+  *sm_count = d->sm_count;
+  *status = d->status;
+  return ATTN_OK;
+}
+
+int record_cuda_error(cudaError_t e) { return record(e); }
+
 }  // namespace attn
 
 extern "C" {
@@ -194,6 +209,7 @@ const char *attn_strerror(int code) {
     case ATTN_ERR_TIMEOUT: return "a bounded device-side wait ran out; outputs undefined";
     case ATTN_ERR_NOMEM: return "could not allocate the split-KV workspace";
     case ATTN_ERR_DEVICE: return "a kernel consistency check failed; outputs undefined";
+    case ATTN_ERR_SCRATCH: return "split-KV partials larger than the fixed scratch of attn_fwd_splitkv_noalloc";
     default: return "unknown attn error code";
   }
 }

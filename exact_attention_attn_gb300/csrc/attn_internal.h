@@ -68,6 +68,11 @@ cudaError_t launch_tc2(const Problem &p, int device, uint64_t wait_limit_ns, cud
 // exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.  Memory-bound, one pass.
 cudaError_t launch_combine(const Problem &p, cudaStream_t stream);
 
+// Current device (as attn_fwd sees it): index, SM count, status word.
+int current_device(int *device, int *sm_count, int **status);
+// Records a CUDA error for attn_last_cuda_error; returns ATTN_ERR_LAUNCH.
+int record_cuda_error(cudaError_t e);
+
 // Plain CUDA-core kernel: correct for every supported shape; used for the
 // shapes the tensor-core kernel does not take.
 cudaError_t launch_simt(const Problem &p, cudaStream_t stream);

@@ -58,6 +58,7 @@ typedef struct CUstream_st *attn_stream_t;
 #define ATTN_ERR_TIMEOUT (-5) /* a kernel's bounded wait ran out (reported by attn_fwd_status) */
 #define ATTN_ERR_NOMEM (-6)   /* the split-KV workspace could not be allocated */
 #define ATTN_ERR_DEVICE (-7)  /* a kernel's own consistency check failed (reported by attn_fwd_status) */
+#define ATTN_ERR_SCRATCH (-8) /* attn_fwd_splitkv_noalloc: the partials need more than ATTN_NOALLOC_SCRATCH_BYTES */
 
 #define ATTN_MAX_HEAD_DIM 1024
 
@@ -113,6 +114,43 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, floa
 ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
                               int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                               float scale, int causal, int kv_splits, attn_stream_t stream);
+
+/*
+ * attn_fwd_splitkv_noalloc -- attn_fwd_splitkv that allocates nothing.
+ *
+ * The pages have no counterpart of this call; it exists for callers that may
+ * not allocate device memory while they run attention: code that owns every
+ * byte of the GPU through its own allocator or memory budget (a serving
+ * process that pins its KV cache and activations up front and must not have
+ * a library take memory behind its back), hard-latency paths where an
+ * allocation -- even a stream-ordered one from a pool that may have to grow --
+ * is an unbounded stall, and callers in contexts where the CUDA allocator
+ * may not be used at all.  Instead of a per-call workspace it uses one
+ * fixed, file-scope device array of ATTN_NOALLOC_SCRATCH_BYTES bytes that
+ * every GPU which loads this library holds until the process exits.
+ *
+ * Arguments are those of attn_fwd_splitkv except that kv_splits must be an
+ * explicit count from 2 to 64 (ATTN_ERR_ARG otherwise).  The partials need
+ * kv_splits * B * Hq * Nq * (D + 1) * 4 bytes; a larger problem is refused
+ * with ATTN_ERR_SCRATCH before anything is launched.  Nkv == 0 needs no
+ * partials and runs the plain no-key path.
+ *
+ * Set-up: the first call on a device looks up the array's device address
+ * with cudaGetSymbolAddress (with that device current); make that first call
+ * outside any stream capture.  No call of this function allocates or frees
+ * device memory.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents.  Nothing in it has to start at zero -- each call writes
+ * every partial it later reads -- but two calls whose kernels overlap on the
+ * GPU (different streams, or a second call before the first one's kernels
+ * have finished on another stream) race on the array and corrupt each
+ * other's results; serialise them, e.g. on one stream.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+ATTN_API int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                      int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                                      float scale, int causal, int kv_splits, attn_stream_t stream);
 
 /*
  * attn_fwd_status -- synchronise `stream`, then read and clear the device

@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_strerror(lib):
     assert lib.attn_version() == 100
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         assert lib.attn_strerror(code)
     assert b"unknown" in lib.attn_strerror(-99)
 
