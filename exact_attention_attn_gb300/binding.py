@@ -61,6 +61,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_splitkv.restype = ci
         lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
         lib.attn_fwd_splitkv_noalloc.restype = ci
+        lib.attn_set_debug.argtypes = [ci, ctypes.c_longlong]
+        lib.attn_set_debug.restype = ci
         lib.attn_fwd_status.argtypes = [vp]
         lib.attn_fwd_status.restype = ci
         lib.attn_strerror.argtypes = [ci]
@@ -176,6 +178,13 @@ def attn_fwd_plan(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int, causal: 
     d = {f: getattr(plan, f) for f, _ in AttnPlan._fields_}
     d["path_name"] = PATH_NAMES.get(plan.path, str(plan.path))
     return d
+
+
+def attn_set_debug(flags: int = 0, wait_limit_ns: int = 0) -> None:
+    """Test support: see attn_set_debug in include/attn.h."""
+    rc = load_library().attn_set_debug(int(flags), int(wait_limit_ns))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_set_debug")
 
 
 def attn_fwd_status(stream=None) -> int:

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "attn.h"
@@ -21,6 +22,8 @@ constexpr int kMaxDevices = 64;
 // bounded device-side waits give up after this long (a healthy wait lasts
 // microseconds)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+std::atomic<long long> g_wait_limit_ns{(long long)kWaitLimitNs};
+std::atomic<int> g_debug_flags{0};
 struct DeviceInfo {
   bool ready = false;
   bool arch_ok = false;
@@ -151,7 +154,8 @@ int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaSt
       break;
     case ATTN_PATH_TC:
       p.kv_splits = 1;
-      e = tc2_supports(p.D) ? launch_tc2(p, dev.device, kWaitLimitNs, st) : launch_tc(p, dev.device, kWaitLimitNs, st);
+      e = tc2_supports(p.D) ? launch_tc2(p, dev.device, wait_limit_ns(), st)
+                            : launch_tc(p, dev.device, wait_limit_ns(), st);
       break;
     case ATTN_PATH_TC_SPLITKV: {
       // stream-ordered workspace: allocated and freed on the caller's stream
@@ -164,7 +168,8 @@ int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaSt
       p.kv_splits = plan.kv_splits;
       p.ws_o = static_cast<float *>(ws);
       p.ws_lse = p.ws_o + (int64_t)plan.kv_splits * rows * p.D;
-      e = tc2_supports(p.D) ? launch_tc2(p, dev.device, kWaitLimitNs, st) : launch_tc(p, dev.device, kWaitLimitNs, st);
+      e = tc2_supports(p.D) ? launch_tc2(p, dev.device, wait_limit_ns(), st)
+                            : launch_tc(p, dev.device, wait_limit_ns(), st);
       if (e == cudaSuccess) e = launch_combine(p, st);
       cudaError_t f = cudaFreeAsync(ws, st);
       if (e == cudaSuccess) e = f;
@@ -193,6 +198,9 @@ int current_device(int *device, int *sm_count, int **status) {
 
 int record_cuda_error(cudaError_t e) { return record(e); }
 
+uint64_t wait_limit_ns() { return (uint64_t)g_wait_limit_ns.load(std::memory_order_relaxed); }
+int debug_flags() { return g_debug_flags.load(std::memory_order_relaxed); }
+
 }  // namespace attn
 
 extern "C" {
@@ -215,6 +223,14 @@ const char *attn_strerror(int code) {
 }
 
 const char *attn_last_cuda_error(void) { return attn::t_last_error; }
+
+int attn_set_debug(int flags, long long wait_limit_ns) {
+  if (flags & ~ATTN_DEBUG_DROP_V_COPY) return ATTN_ERR_ARG;
+  if (wait_limit_ns < 0) return ATTN_ERR_ARG;
+  attn::g_debug_flags.store(flags);
+  attn::g_wait_limit_ns.store(wait_limit_ns == 0 ? (long long)attn::kWaitLimitNs : wait_limit_ns);
+  return ATTN_OK;
+}
 
 int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
                      int B, int Hq, int Hkv, int Nq, int Nkv, int D,
@@ -244,6 +260,7 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float
   p.causal = causal;
   p.status = dev->status;
   p.kv_splits = 1;
+  p.debug_flags = debug_flags();
 
   attn_plan plan;
   make_plan(p, *dev, kv_splits, &plan);

@@ -27,6 +27,10 @@ struct Problem {
   int kv_splits;
   float *ws_o;
   float *ws_lse;
+  // test support (attn_set_debug): bit 0 makes the V producer of the
+  // two-tile kernel skip its copy of the second key block, so that the MMA
+  // thread's bounded wait for it runs out
+  int debug_flags;
 };
 
 // Device status codes written by kernels (same values as the public ATTN_ERR_*).
@@ -67,6 +71,10 @@ cudaError_t launch_tc2(const Problem &p, int device, uint64_t wait_limit_ns, cud
 // Merge kv_splits partial results into o (bf16) and lse: LSE = ln sum_s
 // exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.  Memory-bound, one pass.
 cudaError_t launch_combine(const Problem &p, cudaStream_t stream);
+
+// Bound on device-side waits and debug flags currently set by attn_set_debug.
+uint64_t wait_limit_ns();
+int debug_flags();
 
 // Current device (as attn_fwd sees it): index, SM count, status word.
 int current_device(int *device, int *sm_count, int **status);

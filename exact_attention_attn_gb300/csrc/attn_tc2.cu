@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && nblk > 0) {
       const bool is_k = warp == WARP_LOAD_K;
       uint32_t ctr = 0;
+      uint32_t skipped = 0xffffffffu;  // a copy never issued (test support)
       bool ok = true;
       if (is_k) {
         tma_prefetch_desc(&tm_q);
@@ -225,6 +226,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_v, 0, (jb + j + kPrefetch) * BN, 0, bkv);
           const int vs = ctr % prm.vst;
           if (!mbar_wait(&bars->v_empty[vs], ((ctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+          if ((p.debug_flags & 1) && j == 1) {  // test support: leave this slot empty
+            skipped = ctr;
+            ++ctr;
+            continue;
+          }
           mbar_arrive_expect_tx(&bars->v_full[vs], NC * CHUNK_BYTES);
           tma_load_4d(sv + vs * NC * CHUNK_BYTES, &tm_v, &bars->v_full[vs], 0, (jb + j) * BN, 0, bkv);
           ATTN_TRACE_EV(14, j);
@@ -239,7 +245,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (uint32_t i = ctr - kn; i < ctr; ++i) mbar_wait_drain(&bars->k_full[i % prm.kst], (i / prm.kst) & 1, limit);
       } else {
         const uint32_t vn = ctr < (uint32_t)prm.vst ? ctr : (uint32_t)prm.vst;
-        for (uint32_t i = ctr - vn; i < ctr; ++i) mbar_wait_drain(&bars->v_full[i % prm.vst], (i / prm.vst) & 1, limit);
+        for (uint32_t i = ctr - vn; i < ctr; ++i)
+          if (i != skipped) mbar_wait_drain(&bars->v_full[i % prm.vst], (i / prm.vst) & 1, limit);
       }
     }
   } else if (warp == WARP_MMA) {

@@ -161,6 +161,23 @@ ATTN_API int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *
  */
 ATTN_API int attn_fwd_status(attn_stream_t stream);
 
+/*
+ * attn_set_debug -- test support for the failure path; process-wide, read at
+ * every later launch.
+ *
+ * flags: 0 or ATTN_DEBUG_DROP_V_COPY, which makes the V producer of the
+ *   head-dim-64/128 kernel skip its copy of each CTA's second key block, so
+ *   the MMA thread's wait for it runs out: the kernel then records
+ *   ATTN_ERR_TIMEOUT in the status word, every role of the CTA stops waiting,
+ *   drains its own copies and MMAs, frees its tensor memory and exits (no
+ *   trap, no hang; outputs of that call are undefined).
+ * wait_limit_ns: bound on every device-side wait; 0 restores the default
+ *   (2 s).
+ * Returns ATTN_OK or ATTN_ERR_ARG.
+ */
+#define ATTN_DEBUG_DROP_V_COPY 1
+ATTN_API int attn_set_debug(int flags, long long wait_limit_ns);
+
 /* Static description of a return code. */
 ATTN_API const char *attn_strerror(int code);
 

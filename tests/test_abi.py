@@ -98,6 +98,14 @@ def test_splitkv_argument_errors(lib):
     assert lib.attn_fwd_splitkv(None, None, None, None, None, 0, 2, 1, 8, 8, 64, 0.125, 0, 2, None) == 0
 
 
+def test_set_debug_arguments(lib):
+    lib.attn_set_debug.argtypes = [ctypes.c_int, ctypes.c_longlong]
+    assert lib.attn_set_debug(2, 0) == -1
+    assert lib.attn_set_debug(0, -5) == -1
+    assert lib.attn_set_debug(1, 1000000) == 0
+    assert lib.attn_set_debug(0, 0) == 0
+
+
 def test_missing_library_fails_loudly(tmp_path):
     code = ("import exact_attention_attn_gb300 as A\n"
             "try:\n    A.attn_version()\nexcept ImportError as e:\n    print('RAISED', e)\n")
