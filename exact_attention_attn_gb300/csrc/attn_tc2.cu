@@ -82,6 +82,11 @@ constexpr int kPrefetch = ATTN_TC2_PREFETCH;  // L2 prefetch distance in blocks
 #define ATTN_TC2_POLY_PAIRS 0x52
 #endif
 constexpr unsigned kPolyPairs = ATTN_TC2_POLY_PAIRS;
+#ifdef ATTN_TC2_MMA_SPIN
+#define MMA_WAIT mbar_wait_spin
+#else
+#define MMA_WAIT mbar_wait
+#endif
 constexpr int kSmemMax = 232448;
 
 struct Params2 {
@@ -255,12 +260,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
       const uint32_t sq_addr = smem_u32(sq), sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
-      bool ok = mbar_wait(&bars->q_full, 0, abortf, limit);
+      bool ok = MMA_WAIT(&bars->q_full, 0, abortf, limit);
       // S_t,blk = Q_t K_blk^T.  K block blk sits in ring slot blk % kst; Q tile t
       // chunk c at sq + c*32 KB + t*16 KB (one 256-row copy per chunk).
       auto issue_s = [&](int t, int blk, bool wait_full, bool release) -> bool {
         const int s = blk % prm.kst;
-        if (wait_full && !mbar_wait(&bars->k_full[s], (blk / prm.kst) & 1, abortf, limit)) return false;
+        if (wait_full && !MMA_WAIT(&bars->k_full[s], (blk / prm.kst) & 1, abortf, limit)) return false;
         if (wait_full) ATTN_TRACE_EV(12, blk);
         tc_fence_after();
         // descriptor of a K-major 128B-swizzled chunk; the K=16 step inside a
@@ -284,13 +289,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = 0; j < nblk && ok; ++j) {
         const int vs = j % prm.vst;
         ATTN_TRACE_EV(10, j);
-        if (!mbar_wait(&bars->v_full[vs], (j / prm.vst) & 1, abortf, limit)) { ok = false; break; }
+        if (!MMA_WAIT(&bars->v_full[vs], (j / prm.vst) & 1, abortf, limit)) { ok = false; break; }
         ATTN_TRACE_EV(11, j);
         const uint32_t vaddr = sv_addr + vs * NC * CHUNK_BYTES;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!act(t, j)) continue;
-          if (!mbar_wait(&bars->p_full[t], j & 1, abortf, limit)) { ok = false; break; }
+          if (!MMA_WAIT(&bars->p_full[t], j & 1, abortf, limit)) { ok = false; break; }
           ATTN_TRACE_EV(8 + t, j);
           tc_fence_after();
           const uint64_t vd0 = smem_desc(vaddr, CHUNK_BYTES, 1024);
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, vd0 + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                    (j > 0 || kk > 0) ? 1u : 0u);
+          if (t == 0) ATTN_TRACE_EV(18, j);
           if (j == nblk_t[t] - 1) mma_commit(&bars->o_done[t]);
           if (act(t, j + 1)) {
             const bool first = (t == 0) || !act(0, j + 1);
