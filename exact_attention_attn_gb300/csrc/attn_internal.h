@@ -46,14 +46,17 @@ bool make_tile_map(CUtensorMap *m, const void *base, int cols, int rows, int pla
 // the 128-byte swizzle.  One copy moves a whole K or V block: large copies
 // keep more bytes in flight per TMA operation.
 bool make_block_map(CUtensorMap *m, const void *base, int cols, int rows, int planes, int box_rows);
+// Same view, box of box_chunks chunks starting at the chunk coordinate given
+// to the copy (chunks past the last one read as zeros).
+bool make_chunk_map(CUtensorMap *m, const void *base, int cols, int rows, int planes, int box_rows, int box_chunks);
 
 // Shared-memory plan of the tensor-core kernel for head dim D.
 struct TcConfig {
   int nc;       // 64-column chunks of D
   int nslices;  // output slices (each <= 256 columns)
   int vmax;     // chunks in the widest slice
-  int qres;     // Q tile resident in shared memory
-  int kst;      // K-ring depth (16 KB chunks)
+  int qres;     // Q tile resident in shared memory (else streamed through the ring)
+  int kst;      // Q/K ring depth (32 KB slots of two chunks)
   int vst;      // V-ring depth (slices)
   uint32_t off_q, off_k, off_v, off_bar;
   int smem_bytes;

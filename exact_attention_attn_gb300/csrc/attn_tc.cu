@@ -16,17 +16,19 @@
 // slices of at most 256 columns (the TMEM accumulator budget), each slice a
 // separate CTA that recomputes the scores.
 //
-// CTA = 6 warps:
+// CTA = 8 warps:
 //   warps 0-3  softmax + correction + epilogue, one query row per thread
 //              (warp w may only touch TMEM lanes 32w..32w+31)
-//   warp 4     TMA producer (one thread)
+//   warps 4, 6 TMA producers of the Q/K ring (one thread each, alternate
+//              ring positions; every copy moves two 64-column chunks, 32 KB)
 //   warp 5     TMEM allocator and MMA issuer (one thread)
+//   warp 7     TMA producer of V (one copy of the block's output slice)
 //
 // TMEM columns: S [0,128) fp32 scores; P0 [128,192) and P1 [192,256) bf16
 // pairs (double-buffered); O [256, 256+DV) fp32 output slice.
 //
 // Synchronisation (mbarriers; every wait is bounded):
-//   k_full/k_empty, v_full/v_empty   TMA ring <-> MMA
+//   k_full/k_empty, v_full/v_empty   TMA rings <-> MMA
 //   s_full   MMA -> softmax (S_j ready)       s_free  softmax -> MMA (S read)
 //   p_full[2] softmax -> MMA (P_j in TMEM)    o_bar[2] MMA -> softmax (PV_j done)
 // MMA issue order is S_0, S_1, PV_0, S_2, PV_1, ...; tcgen05.commit after S_j
@@ -50,9 +52,12 @@ using namespace ptx;
 constexpr int BM = 128;                  // query rows per tile (MMA M)
 constexpr int BN = 128;                  // keys per block (MMA N of S, K of PV)
 constexpr int CHUNK_BYTES = 128 * 128;   // one 128-row x 64-col bf16 tile
-constexpr int THREADS = 192;
-constexpr int WARP_LOAD = 4;
+constexpr int THREADS = 256;
+constexpr int WARP_LOAD_QK0 = 4;
 constexpr int WARP_MMA = 5;
+constexpr int WARP_LOAD_QK1 = 6;
+constexpr int WARP_LOAD_V = 7;
+constexpr int SLOT_BYTES = 2 * 128 * 128;  // Q/K ring slot: two 128-row x 64-col chunks
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0, TM_P0 = 128, TM_P1 = 192, TM_O = 256;
 constexpr float TAU = 8.0f;              // rescale threshold, log2 units
@@ -65,7 +70,8 @@ struct TcParams {
   int nc;        // contraction chunks = D / 64
   int nslices;   // output slices
   int ntiles;    // query tiles per head
-  int kst, vst;  // ring depths (K ring in 16 KB chunks; V ring in slices)
+  int kst, vst;  // ring depths (Q/K ring in 32 KB slots; V ring in slices)
+  int npairs;    // chunk pairs per block (ceil(nc / 2))
   int qres;      // Q resident in shared memory (else streamed through the K ring)
   int vmax;      // chunks in the widest output slice
   uint32_t off_q, off_k, off_v, off_bar;
@@ -84,6 +90,7 @@ struct Bars {
   uint64_t done;
   uint32_t tmem_slot;
   int abort;
+  int slot_item[MAX_KST];  // last Q/K item issued into each ring slot
 };
 
 __device__ __forceinline__ void raise_abort(Bars *bars, int *status) {
@@ -94,6 +101,8 @@ __device__ __forceinline__ void raise_abort(Bars *bars, int *status) {
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+  // tm_q: 128-row boxes of all chunks when Q is resident, else of two chunks;
+  // tm_k: 128-row boxes of two chunks; tm_v: 128-row boxes of vmax chunks
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -153,6 +162,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bars->o_bar[1], 1);
     mbar_init(&bars->done, 1);
     bars->abort = 0;
+    for (int i = 0; i < MAX_KST; ++i) bars->slot_item[i] = -1;
     fence_mbar_init();
   }
   if (warp == WARP_MMA) {
@@ -164,47 +174,59 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
-  if (warp == WARP_LOAD) {
-    // ------------------------------------------------------------ producer
+  // Q/K ring items: per block, for each chunk pair c2: [Q pair c2 if Q is
+  // streamed], K pair c2.  Item i sits in slot i % kst; producer (i % 2).
+  const int items_pb = prm.qres ? prm.npairs : 2 * prm.npairs;
+  if (warp == WARP_LOAD_QK0 || warp == WARP_LOAD_QK1) {
+    // ------------------------------------------------------------ Q/K producers
+    const int r = (warp == WARP_LOAD_QK0) ? 0 : 1;
     if (lane == 0 && nblk > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      uint32_t kctr = 0, vctr = 0;
       bool ok = true;
-      if (prm.qres) {
-        mbar_arrive_expect_tx(&bars->q_full, prm.nc * CHUNK_BYTES);
-        for (int c = 0; c < prm.nc; ++c) tma_load_3d(sq + c * CHUNK_BYTES, &tm_q, &bars->q_full, c * 64, q0, bh);
-      }
-      for (int j = 0; j < nblk && ok; ++j) {
-        for (int c = 0; c < prm.nc && ok; ++c) {
-          if (!prm.qres) {
-            const int s = kctr % prm.kst;
-            if (!mbar_wait(&bars->k_empty[s], ((kctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
-            mbar_arrive_expect_tx(&bars->k_full[s], CHUNK_BYTES);
-            tma_load_3d(sk + s * CHUNK_BYTES, &tm_q, &bars->k_full[s], c * 64, q0, bh);
-            ++kctr;
-          }
-          const int s = kctr % prm.kst;
-          if (!mbar_wait(&bars->k_empty[s], ((kctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->k_full[s], CHUNK_BYTES);
-          tma_load_3d(sk + s * CHUNK_BYTES, &tm_k, &bars->k_full[s], c * 64, (jb + j) * BN, bkv);
-          ++kctr;
+      if (r == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        if (prm.qres) {
+          mbar_arrive_expect_tx(&bars->q_full, prm.nc * CHUNK_BYTES);
+          tma_load_4d(sq, &tm_q, &bars->q_full, 0, q0, 0, bh);
         }
-        if (!ok) break;
+      }
+      const int total = nblk * items_pb;
+      for (int i = r; i < total; i += 2) {
+        const int s = i % prm.kst;
+        if (!mbar_wait(&bars->k_empty[s], ((i / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+        const int j = i / items_pb, m = i % items_pb;
+        const bool is_q = !prm.qres && (m & 1) == 0;
+        const int c2 = prm.qres ? m : (m >> 1);
+        mbar_arrive_expect_tx(&bars->k_full[s], SLOT_BYTES);
+        *reinterpret_cast<volatile int *>(&bars->slot_item[s]) = i;
+        if (is_q)
+          tma_load_4d(sk + s * SLOT_BYTES, &tm_q, &bars->k_full[s], 0, q0, 2 * c2, bh);
+        else
+          tma_load_4d(sk + s * SLOT_BYTES, &tm_k, &bars->k_full[s], 0, (jb + j) * BN, 2 * c2, bkv);
+      }
+      if (!ok) raise_abort(bars, p.status);
+      // drain: copies of this thread that are still the latest in their slot
+      // may be in flight; every older one was consumed before its slot refilled
+      if (r == 0 && prm.qres) mbar_wait_drain(&bars->q_full, 0, limit);
+      for (int s = 0; s < prm.kst; ++s) {
+        const int i = *reinterpret_cast<volatile int *>(&bars->slot_item[s]);
+        if (i >= 0 && (i & 1) == r) mbar_wait_drain(&bars->k_full[s], (i / prm.kst) & 1, limit);
+      }
+    }
+  } else if (warp == WARP_LOAD_V) {
+    // ------------------------------------------------------------ V producer
+    if (lane == 0 && nblk > 0) {
+      tma_prefetch_desc(&tm_v);
+      uint32_t vctr = 0;
+      bool ok = true;
+      for (int j = 0; j < nblk; ++j) {
         const int vs = vctr % prm.vst;
         if (!mbar_wait(&bars->v_empty[vs], ((vctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars->v_full[vs], s_chunks * CHUNK_BYTES);
-        uint8_t *vdst = sv + vs * (prm.vmax * CHUNK_BYTES);
-        for (int c = 0; c < s_chunks; ++c)
-          tma_load_3d(vdst + c * CHUNK_BYTES, &tm_v, &bars->v_full[vs], (s_c0 + c) * 64, (jb + j) * BN, bkv);
+        mbar_arrive_expect_tx(&bars->v_full[vs], prm.vmax * CHUNK_BYTES);
+        tma_load_4d(sv + vs * (prm.vmax * CHUNK_BYTES), &tm_v, &bars->v_full[vs], 0, (jb + j) * BN, s_c0, bkv);
         ++vctr;
       }
       if (!ok) raise_abort(bars, p.status);
-      // drain: every copy this thread issued must land before the CTA exits
-      if (prm.qres) mbar_wait_drain(&bars->q_full, 0, limit);
-      const uint32_t kn = kctr < (uint32_t)prm.kst ? kctr : (uint32_t)prm.kst;
-      for (uint32_t i = kctr - kn; i < kctr; ++i) mbar_wait_drain(&bars->k_full[i % prm.kst], (i / prm.kst) & 1, limit);
       const uint32_t vn = vctr < (uint32_t)prm.vst ? vctr : (uint32_t)prm.vst;
       for (uint32_t i = vctr - vn; i < vctr; ++i) mbar_wait_drain(&bars->v_full[i % prm.vst], (i / prm.vst) & 1, limit);
     }
@@ -214,30 +236,33 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(BM, DV, 0, 1);
       const uint32_t sq_addr = smem_u32(sq), sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
-      uint32_t kctr = 0, vctr = 0;
+      uint32_t vctr = 0;
+      int item = 0;  // next Q/K ring item
       bool ok = true;
       if (prm.qres) ok = mbar_wait(&bars->q_full, 0, abortf, limit);
       auto issue_s = [&]() -> bool {
-        for (int c = 0; c < prm.nc; ++c) {
-          uint32_t qaddr;
+        for (int c2 = 0; c2 < prm.npairs; ++c2) {
+          uint32_t qaddr = 0;
           int qslot = -1;
-          if (prm.qres) {
-            qaddr = sq_addr + c * CHUNK_BYTES;
-          } else {
-            qslot = kctr % prm.kst;
-            if (!mbar_wait(&bars->k_full[qslot], (kctr / prm.kst) & 1, abortf, limit)) return false;
-            qaddr = sk_addr + qslot * CHUNK_BYTES;
-            ++kctr;
+          if (!prm.qres) {
+            qslot = item % prm.kst;
+            if (!mbar_wait(&bars->k_full[qslot], (item / prm.kst) & 1, abortf, limit)) return false;
+            qaddr = sk_addr + qslot * SLOT_BYTES;
+            ++item;
           }
-          const int ks = kctr % prm.kst;
-          if (!mbar_wait(&bars->k_full[ks], (kctr / prm.kst) & 1, abortf, limit)) return false;
-          const uint32_t kaddr = sk_addr + ks * CHUNK_BYTES;
-          ++kctr;
+          const int ks = item % prm.kst;
+          if (!mbar_wait(&bars->k_full[ks], (item / prm.kst) & 1, abortf, limit)) return false;
+          const uint32_t kaddr = sk_addr + ks * SLOT_BYTES;
+          ++item;
           tc_fence_after();
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * c2 + cc;
+            if (c >= prm.nc) break;
+            const uint32_t qa = prm.qres ? sq_addr + c * CHUNK_BYTES : qaddr + cc * CHUNK_BYTES;
+            const uint64_t qd = smem_desc(qa, 16, 1024), kd = smem_desc(kaddr + cc * CHUNK_BYTES, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + TM_S, smem_desc(qaddr + kk * 32, 16, 1024), smem_desc(kaddr + kk * 32, 16, 1024), idesc_s,
-                   (c | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + TM_S, qd + kk * 2, kd + kk * 2, idesc_s, (c | kk) != 0);
+          }
           mma_commit(&bars->k_empty[ks]);
           if (qslot >= 0) mma_commit(&bars->k_empty[qslot]);
         }
@@ -441,19 +466,23 @@ TcConfig tc_config(int D) {
   c.vmax = (c.nc + c.nslices - 1) / c.nslices;
   const int avail = kSmemMax - kSmemReserve;
   const int qb = c.nc * CHUNK_BYTES, vb = c.vmax * CHUNK_BYTES;
-  c.qres = qb + 2 * CHUNK_BYTES + vb <= avail;
-  if (c.qres) {
-    c.vst = (avail - qb - 2 * CHUNK_BYTES >= 2 * vb) ? 2 : 1;
-    c.kst = (avail - qb - c.vst * vb) / CHUNK_BYTES;
+  // Q resident when it leaves room for at least three Q/K slots and one V
+  // slot (two V slots if three Q/K slots still fit); else Q streams through
+  // the ring next to K, with two V slots when four ring slots remain
+  c.qres = 0;
+  c.vst = 1;
+  if (qb + vb + 3 * SLOT_BYTES <= avail) {
+    c.qres = 1;
+    c.vst = (qb + 2 * vb + 3 * SLOT_BYTES <= avail) ? 2 : 1;
+    c.kst = (avail - qb - c.vst * vb) / SLOT_BYTES;
   } else {
-    c.vst = (avail - 4 * CHUNK_BYTES >= 2 * vb) ? 2 : 1;
-    c.kst = (avail - c.vst * vb) / CHUNK_BYTES;
-    c.kst &= ~1;
+    c.vst = (2 * vb + 4 * SLOT_BYTES <= avail) ? 2 : 1;
+    c.kst = (avail - c.vst * vb) / SLOT_BYTES;
   }
   if (c.kst > MAX_KST) c.kst = MAX_KST;
   c.off_q = 0;
   c.off_k = c.qres ? qb : 0;
-  c.off_v = c.off_k + c.kst * CHUNK_BYTES;
+  c.off_v = c.off_k + c.kst * SLOT_BYTES;
   c.off_bar = c.off_v + c.vst * vb;
   c.smem_bytes = c.off_bar + (int)sizeof(Bars) + 1024;  // + alignment slack
   return c;
@@ -464,9 +493,9 @@ cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cuda
   const TcConfig c = tc_config(p.D);
   if (c.kst < 2 || c.smem_bytes > kSmemMax) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
-  if (!make_tile_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq)) return cudaErrorInvalidValue;
-  if (!make_tile_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
-  if (!make_tile_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq, BM, c.qres ? c.nc : 2)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv, BN, 2)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv, BN, c.vmax)) return cudaErrorInvalidValue;
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.p = p;
@@ -477,6 +506,7 @@ cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cuda
   prm.vst = c.vst;
   prm.qres = c.qres;
   prm.vmax = c.vmax;
+  prm.npairs = (c.nc + 1) / 2;
   prm.off_q = c.off_q;
   prm.off_k = c.off_k;
   prm.off_v = c.off_v;
