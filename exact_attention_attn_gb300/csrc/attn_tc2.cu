@@ -420,15 +420,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         // every key visible and scale > 0: y = s*sl2 - mu on f32x2 pairs;
         // 3 of every 8 pairs take exp2 on the FMA pipe, the rest on the MUFU,
         // so that neither unit alone bounds the block
+        // The scores are read again from TMEM a quarter at a time (the next
+        // quarter's load in flight while this one is turned into P), so only
+        // 64 of them are live here: P quarter h lands in columns [16h, 16h+16),
+        // already read, while the load in flight reads [32(h+1), 32(h+2)).
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nmu2 = f2_pack(-mu, -mu);
         uint64_t acc0 = 0ull, acc1 = 0ull;
+        uint32_t qbuf[2][32];
+        tmem_ld32(tS, qbuf[0]);
+        tmem_wait_ld();
+        reg_fence32(qbuf[0]);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
+          uint32_t(&cur)[32] = qbuf[h & 1];
+          if (h < 3) tmem_ld32(tS + 32 * (h + 1), qbuf[(h + 1) & 1]);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int q = h * 16 + i;
-            const uint64_t y = f2_fma(f2_pack(x[2 * q], x[2 * q + 1]), sl2x2, nmu2);
+            const uint64_t y =
+                f2_fma(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), sl2x2, nmu2);
             uint64_t p2;
             if ((kPolyPairs >> (q & 7)) & 1) {
               p2 = exp2_poly(y);
@@ -446,6 +457,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + h * 16, pk);
+          if (h < 3) {
+            tmem_wait_ld();
+            reg_fence32(qbuf[(h + 1) & 1]);
+          }
         }
         float a0, a1, b0, b1;
         f2_unpack(acc0, a0, a1);
