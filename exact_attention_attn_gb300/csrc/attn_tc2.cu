@@ -77,9 +77,10 @@ constexpr int MAX_KST = 8, MAX_VST = 3;
 #define ATTN_TC2_PREFETCH 0
 #endif
 constexpr int kPrefetch = ATTN_TC2_PREFETCH;  // L2 prefetch distance in blocks
-// pairs q with bit (q % 8) set take the FMA-pipe exp2 (3 of 8)
+// pairs q with bit (q % 8) set take the FMA-pipe exp2 (none by default: the
+// MUFU ex2 alone is faster at the current balance of the softmax warps)
 #ifndef ATTN_TC2_POLY_PAIRS
-#define ATTN_TC2_POLY_PAIRS 0x52
+#define ATTN_TC2_POLY_PAIRS 0
 #endif
 constexpr unsigned kPolyPairs = ATTN_TC2_POLY_PAIRS;
 #ifdef ATTN_TC2_MMA_SPIN
