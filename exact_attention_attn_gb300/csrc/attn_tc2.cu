@@ -34,17 +34,21 @@
 #include "attn_internal.h"
 #include "sm100_ptx.cuh"
 
-// Optional per-role timestamps (clock64) for the first 8 CTAs, compiled in
-// only when ATTN_TRACE is defined: ATTN_TRACE_EV(row, col) stores into the
-// caller-provided buffer attn_trace_buf[cta][24][64] (pointer read once per
-// thread by ATTN_TRACE_SETUP).
+// Optional per-role timestamps (clock64) for 8 CTAs starting at
+// attn_trace_first, compiled in only when ATTN_TRACE is defined:
+// ATTN_TRACE_EV(row, col) stores into the caller-provided buffer
+// attn_trace_buf[cta - attn_trace_first][32][64] (pointer read once per thread
+// by ATTN_TRACE_SETUP).
 #ifdef ATTN_TRACE
 __device__ long long *attn_trace_buf;
-#define ATTN_TRACE_SETUP long long *const attn_tbuf = (blockIdx.x < 8) ? attn_trace_buf : nullptr
+__device__ unsigned attn_trace_first;
+#define ATTN_TRACE_SETUP                                                           \
+  const unsigned attn_tcta = blockIdx.x - attn_trace_first;                       \
+  long long *const attn_tbuf = (attn_tcta < 8u) ? attn_trace_buf : nullptr
 #define ATTN_TRACE_EV(row, col)                                                              \
   do {                                                                                       \
     const long long _t = clock64();                                                          \
-    if (attn_tbuf && (col) < 64) attn_tbuf[((long long)blockIdx.x * 24 + (row)) * 64 + (col)] = _t; \
+    if (attn_tbuf && (col) < 64) attn_tbuf[((long long)attn_tcta * 32 + (row)) * 64 + (col)] = _t; \
   } while (0)
 #else
 #define ATTN_TRACE_SETUP \
@@ -52,6 +56,24 @@ __device__ long long *attn_trace_buf;
   } while (0)
 #define ATTN_TRACE_EV(row, col) \
   do {                          \
+  } while (0)
+#endif
+// Optional per-CTA start/end stamps (globaltimer ns) and SM id, compiled in
+// only when ATTN_TRACE_CTA is defined: attn_cta_buf[cta][4] = {start, end, sm}.
+#ifdef ATTN_TRACE_CTA
+__device__ long long *attn_cta_buf;
+#define ATTN_CTA_EV(slot)                                                                          \
+  do {                                                                                             \
+    if (threadIdx.x == 0 && attn_cta_buf) {                                                        \
+      uint32_t _sm;                                                                                \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(_sm));                                             \
+      attn_cta_buf[(long long)blockIdx.x * 4 + (slot)] = (long long)ptx::globaltimer_ns();          \
+      attn_cta_buf[(long long)blockIdx.x * 4 + 2] = _sm;                                           \
+    }                                                                                              \
+  } while (0)
+#else
+#define ATTN_CTA_EV(slot) \
+  do {                    \
   } while (0)
 #endif
 
@@ -135,6 +157,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t limit = prm.wait_limit_ns;
   ATTN_TRACE_SETUP;
+  ATTN_CTA_EV(0);
+  if (tid == 0) ATTN_TRACE_EV(19, 0);
 
   // ---- work unit: (b, hq) fastest, then tile pair (heaviest causal pairs first)
   const int BH = p.B * p.Hq;
@@ -262,6 +286,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
       const uint32_t sq_addr = smem_u32(sq), sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
       bool ok = MMA_WAIT(&bars->q_full, 0, abortf, limit);
+      ATTN_TRACE_EV(25, 0);
       // S_t,blk = Q_t K_blk^T.  K block blk sits in ring slot blk % kst; Q tile t
       // chunk c at sq + c*32 KB + t*16 KB (one 256-row copy per chunk).
       auto issue_s = [&](int t, int blk, bool wait_full, bool release) -> bool {
@@ -418,9 +443,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the branch must be warp-uniform: both sides end in the warp-collective
       // tcgen05.st, which every lane of the warp has to execute together
       if (__all_sync(0xffffffffu, pos && full)) {
-        // every key visible and scale > 0: y = s*sl2 - mu on f32x2 pairs;
-        // 3 of every 8 pairs take exp2 on the FMA pipe, the rest on the MUFU,
-        // so that neither unit alone bounds the block
+        // every key visible and scale > 0: y = s*sl2 - mu on f32x2 pairs,
+        // exp2 on the MUFU (pairs selected by kPolyPairs on the FMA pipe)
         // The scores are read again from TMEM a quarter at a time (the next
         // quarter's load in flight while this one is turned into P), so only
         // 64 of them are live here: P quarter h lands in columns [16h, 16h+16),
@@ -504,6 +528,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         raise_abort(bars, p.status);
         ok = false;
       }
+      if (tr) ATTN_TRACE_EV(21 + t, 0);
     }
     if (ok) {
       tc_fence_after();
@@ -565,8 +590,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
+  if ((tid & 127) == 0 && warp < 8) ATTN_TRACE_EV(23 + (warp >> 2), 0);
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) ATTN_TRACE_EV(20, 0);
+  ATTN_CTA_EV(1);
   if (warp == WARP_MMA) {
     __syncwarp();
     tc_fence_after();
