@@ -85,6 +85,23 @@ def test_fully_masked_rows():
     assert torch.all(o[:, :, :200] == 0) and torch.all(torch.isneginf(l[:, :, :200]))
 
 
+@pytest.mark.parametrize("Nq", [1, 129, 300])
+@pytest.mark.parametrize("D", [64, 128])
+def test_no_write_past_output(Nq, D):
+    # O and LSE as the leading slice of larger sentinel-filled buffers: the
+    # kernel's stores (row-clipped tile copies for O) must stay inside them
+    B, Hq, Hkv = 2, 2, 1
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, 257, D, seed=Nq + D)
+    big_o = torch.full((B + 1, Hq, Nq, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    big_l = torch.full((B + 1, Hq, Nq), 7.0, dtype=torch.float32, device="cuda")
+    out, lse = big_o[:B], big_l[:B]
+    attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=D ** -0.5, causal=True, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(big_o[B] == 7.0) and torch.all(big_l[B] == 7.0)
+    mx, mean, dl = compare(out.cpu(), lse.cpu(), q, k, v, D ** -0.5, True)
+    assert mx <= 2e-2 and mean <= 2e-3 and dl <= 1e-3, (mx, mean, dl)
+
+
 def test_deterministic():
     q, k, v = (t.cuda() for t in make_qkv(2, 4, 2, 777, 777, 128, 21))
     o1, l1 = attn_fwd(q, k, v, causal=True)
