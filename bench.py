@@ -126,30 +126,43 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # ncu traffic recorded in profiles/ (null when the kernel source changed since)
 
-def kernel_source_hash() -> str:
+# The sources a kernel's code and launch depend on: its own translation unit
+# plus the shared headers, the tensor-map builder and the launch planner.
+_COMMON_SOURCES = ("attn_internal.h", "sm100_ptx.cuh", "tma_host.cu", "attn_api.cu")
+KERNEL_SOURCES = {
+    "attn_tc2_kernel": ("attn_tc2.cu",) + _COMMON_SOURCES,
+    "attn_tc_kernel": ("attn_tc.cu",) + _COMMON_SOURCES,
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """First 16 hex digits of sha256 over the named kernel's source files."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_attn_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+    for f in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """Parse profiles/ncu_traffic.md rows: | workload | kernel | source hash | bytes per launch |"""
+    """Parse profiles/ncu_traffic.md rows: | workload | kernel | source hash | bytes per launch |.
+    A row counts only while its kernel's sources still hash to its value."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
     if not os.path.exists(path):
         return None, None
-    cur = kernel_source_hash()
     for line in open(path):
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 4 and cells[0] == workload and cells[2] == cur:
-            try:
-                return float(cells[3]), cells[1]
-            except ValueError:
-                pass
+        if len(cells) < 4 or cells[0] != workload:
+            continue
+        base = cells[1].split("<")[0]
+        if base not in KERNEL_SOURCES or cells[2] != kernel_source_hash(base):
+            continue
+        try:
+            return float(cells[3]), cells[1]
+        except ValueError:
+            pass
     return None, None
 
 
