@@ -56,6 +56,7 @@ struct TcConfig {
   int nslices;  // output slices (each <= 256 columns)
   int vmax;     // chunks in the widest slice
   int qres;     // Q tile resident in shared memory (else streamed through the ring)
+  int vring;    // V blocks travel through the Q/K ring too (Q resident, no V slot)
   int kst;      // Q/K ring depth (32 KB slots of two chunks)
   int vst;      // V-ring depth (slices)
   uint32_t off_q, off_k, off_v, off_bar;

@@ -22,7 +22,14 @@
 //   warps 4, 6 TMA producers of the Q/K ring (one thread each, alternate
 //              ring positions; every copy moves two 64-column chunks, 32 KB)
 //   warp 5     TMEM allocator and MMA issuer (one thread)
-//   warp 7     TMA producer of V (one copy of the block's output slice)
+//   warp 7     TMA producer of V (one copy of the block's output slice), idle
+//              when V travels through the ring
+//
+// Shared memory, by head dim: Q resident plus the ring plus a V slot (small
+// D); Q resident and V in the ring as 32 KB items next to K (D = 384..512,
+// where Q and a V slot do not both fit: streaming Q again for every key
+// block would add 128 KB per block to an operand stream that the TMA cannot
+// sustain); Q streamed through the ring (D >= 576, Q alone over 144 KB).
 //
 // TMEM columns: S [0,128) fp32 scores; P0 [128,192) and P1 [192,256) bf16
 // pairs (double-buffered); O [256, 256+DV) fp32 output slice.
@@ -43,6 +50,29 @@
 
 #include "attn_internal.h"
 #include "sm100_ptx.cuh"
+
+// Optional per-role timestamps (clock64) for 8 CTAs starting at
+// attn_tc_trace_first, compiled in only when ATTN_TRACE is defined:
+// TC_TRACE_EV(row, col) stores into attn_tc_trace_buf[cta][32][64].
+#ifdef ATTN_TRACE
+__device__ long long *attn_tc_trace_buf;
+__device__ unsigned attn_tc_trace_first;
+#define TC_TRACE_SETUP                                                       \
+  const unsigned tc_tcta = blockIdx.x - attn_tc_trace_first;                \
+  long long *const tc_tbuf = (tc_tcta < 8u) ? attn_tc_trace_buf : nullptr
+#define TC_TRACE_EV(row, col)                                                                    \
+  do {                                                                                           \
+    const long long _t = clock64();                                                              \
+    if (tc_tbuf && (col) < 64) tc_tbuf[((long long)tc_tcta * 32 + (row)) * 64 + (col)] = _t;   \
+  } while (0)
+#else
+#define TC_TRACE_SETUP \
+  do {                 \
+  } while (0)
+#define TC_TRACE_EV(row, col) \
+  do {                        \
+  } while (0)
+#endif
 
 namespace attn {
 namespace {
@@ -73,6 +103,8 @@ struct TcParams {
   int kst, vst;  // ring depths (Q/K ring in 32 KB slots; V ring in slices)
   int npairs;    // chunk pairs per block (ceil(nc / 2))
   int qres;      // Q resident in shared memory (else streamed through the K ring)
+  int vring;     // V blocks as ring items (2 chunks each) after the next block's K
+  int nvitems;   // ring items per V block when vring: ceil(vmax / 2)
   int vmax;      // chunks in the widest output slice
   uint32_t off_q, off_k, off_v, off_bar;
   uint64_t wait_limit_ns;
@@ -93,6 +125,37 @@ struct Bars {
   int slot_item[MAX_KST];  // last Q/K item issued into each ring slot
 };
 
+// Ring item i when V travels through the ring: the K pairs of block 0, then
+// for each block j the K pairs of block j+1 (while there is one) followed by
+// the V items of block j -- the order in which the MMA thread consumes them
+// (S_0, then S_{j+1} before P_j V_j).
+struct RingItem {
+  bool is_v;
+  int blk, idx;  // key block; chunk pair (K) or V item
+};
+__device__ __forceinline__ RingItem vring_item(int i, int np, int nv, int nblk) {
+  RingItem r;
+  if (i < np) {
+    r.is_v = false;
+    r.blk = 0;
+    r.idx = i;
+    return r;
+  }
+  i -= np;
+  const int g = i / (np + nv), m = i % (np + nv);
+  if (g < nblk - 1 && m < np) {
+    r.is_v = false;
+    r.blk = g + 1;
+    r.idx = m;
+  } else {
+    // V items of block g; in the last group (no K after it) only V items exist
+    r.is_v = true;
+    r.blk = g;
+    r.idx = (g < nblk - 1) ? m - np : i - g * (np + nv);
+  }
+  return r;
+}
+
 __device__ __forceinline__ void raise_abort(Bars *bars, int *status) {
   atomicCAS(status, 0, kStatusTimeout);
   *reinterpret_cast<volatile int *>(&bars->abort) = 1;
@@ -102,7 +165,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
   // tm_q: 128-row boxes of all chunks when Q is resident, else of two chunks;
-  // tm_k: 128-row boxes of two chunks; tm_v: 128-row boxes of vmax chunks
+  // tm_k: 128-row boxes of two chunks; tm_v: 128-row boxes of vmax chunks, or
+  // of two chunks when V travels through the ring
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -115,6 +179,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const Problem &p = prm.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t limit = prm.wait_limit_ns;
+  TC_TRACE_SETUP;
+  if (tid == 0) TC_TRACE_EV(0, 0);
 
   // ---- work unit: output slice fastest, then (b, hq), then query tile
   //      (heaviest causal tiles first)
@@ -176,7 +242,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   // Q/K ring items: per block, for each chunk pair c2: [Q pair c2 if Q is
   // streamed], K pair c2.  Item i sits in slot i % kst; producer (i % 2).
-  const int items_pb = prm.qres ? prm.npairs : 2 * prm.npairs;
+  const int items_pb = prm.qres ? prm.npairs : 2 * prm.npairs;  // when V is not in the ring
   if (warp == WARP_LOAD_QK0 || warp == WARP_LOAD_QK1) {
     // ------------------------------------------------------------ Q/K producers
     const int r = (warp == WARP_LOAD_QK0) ? 0 : 1;
@@ -190,15 +256,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_4d(sq, &tm_q, &bars->q_full, 0, q0, 0, bh);
         }
       }
-      const int total = nblk * items_pb;
+      const int total = prm.vring ? nblk * (prm.npairs + prm.nvitems) : nblk * items_pb;
       for (int i = r; i < total; i += 2) {
         const int s = i % prm.kst;
         if (!mbar_wait(&bars->k_empty[s], ((i / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bars->k_full[s], SLOT_BYTES);
+        *reinterpret_cast<volatile int *>(&bars->slot_item[s]) = i;
+        TC_TRACE_EV(1 + i / 64, i % 64);
+        if (prm.vring) {
+          const RingItem it = vring_item(i, prm.npairs, prm.nvitems, nblk);
+          if (it.is_v)
+            tma_load_4d(sk + s * SLOT_BYTES, &tm_v, &bars->k_full[s], 0, (jb + it.blk) * BN, s_c0 + 2 * it.idx, bkv);
+          else
+            tma_load_4d(sk + s * SLOT_BYTES, &tm_k, &bars->k_full[s], 0, (jb + it.blk) * BN, 2 * it.idx, bkv);
+          continue;
+        }
         const int j = i / items_pb, m = i % items_pb;
         const bool is_q = !prm.qres && (m & 1) == 0;
         const int c2 = prm.qres ? m : (m >> 1);
-        mbar_arrive_expect_tx(&bars->k_full[s], SLOT_BYTES);
-        *reinterpret_cast<volatile int *>(&bars->slot_item[s]) = i;
         if (is_q)
           tma_load_4d(sk + s * SLOT_BYTES, &tm_q, &bars->k_full[s], 0, q0, 2 * c2, bh);
         else
@@ -215,7 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == WARP_LOAD_V) {
     // ------------------------------------------------------------ V producer
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0 && nblk > 0 && !prm.vring) {
       tma_prefetch_desc(&tm_v);
       uint32_t vctr = 0;
       bool ok = true;
@@ -235,36 +310,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && nblk > 0) {
       const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(BM, DV, 0, 1);
-      const uint32_t sq_addr = smem_u32(sq), sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
+      // K-major 128B-swizzled chunk descriptors: a K=16 step adds 32 bytes (2 in
+      // the >>4 address field), a chunk 16 KB, a ring slot 32 KB
+      constexpr uint64_t kChunkD = CHUNK_BYTES >> 4, kSlotD = SLOT_BYTES >> 4;
+      const uint64_t qd_res = smem_desc(smem_u32(sq), 16, 1024);
+      const uint64_t kd_ring = smem_desc(smem_u32(sk), 16, 1024);
+      // V (MN-major): a K=16 step is 16 keys = 2048 bytes; chunks 16 KB apart
+      const uint64_t vd_ring = smem_desc(smem_u32(sk), CHUNK_BYTES, 1024);
+      const uint64_t vd_sep = smem_desc(smem_u32(sv), CHUNK_BYTES, 1024);
+      // ring position of the next Q/K/V item, kept incrementally
+      int slot = 0;
+      uint32_t phase = 0;
+      auto next_item = [&](int &s_out) -> bool {
+        s_out = slot;
+        const bool r = mbar_wait(&bars->k_full[slot], phase, abortf, limit);
+        if (++slot == prm.kst) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        return r;
+      };
       uint32_t vctr = 0;
-      int item = 0;  // next Q/K ring item
       bool ok = true;
       if (prm.qres) ok = mbar_wait(&bars->q_full, 0, abortf, limit);
       auto issue_s = [&]() -> bool {
         for (int c2 = 0; c2 < prm.npairs; ++c2) {
-          uint32_t qaddr = 0;
-          int qslot = -1;
-          if (!prm.qres) {
-            qslot = item % prm.kst;
-            if (!mbar_wait(&bars->k_full[qslot], (item / prm.kst) & 1, abortf, limit)) return false;
-            qaddr = sk_addr + qslot * SLOT_BYTES;
-            ++item;
-          }
-          const int ks = item % prm.kst;
-          if (!mbar_wait(&bars->k_full[ks], (item / prm.kst) & 1, abortf, limit)) return false;
-          const uint32_t kaddr = sk_addr + ks * SLOT_BYTES;
-          ++item;
+          int qs = -1, ks;
+          if (!prm.qres && !next_item(qs)) return false;
+          if (!next_item(ks)) return false;
+          TC_TRACE_EV(5, c2);
           tc_fence_after();
-          for (int cc = 0; cc < 2; ++cc) {
-            const int c = 2 * c2 + cc;
-            if (c >= prm.nc) break;
-            const uint32_t qa = prm.qres ? sq_addr + c * CHUNK_BYTES : qaddr + cc * CHUNK_BYTES;
-            const uint64_t qd = smem_desc(qa, 16, 1024), kd = smem_desc(kaddr + cc * CHUNK_BYTES, 16, 1024);
+          const int ncc = min(2, prm.nc - 2 * c2);
+          const uint64_t qd = prm.qres ? qd_res + (uint64_t)(2 * c2) * kChunkD : kd_ring + (uint64_t)qs * kSlotD;
+          const uint64_t kd = kd_ring + (uint64_t)ks * kSlotD;
+          for (int cc = 0; cc < ncc; ++cc) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + TM_S, qd + kk * 2, kd + kk * 2, idesc_s, (c | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + TM_S, qd + cc * kChunkD + kk * 2, kd + cc * kChunkD + kk * 2, idesc_s, (c2 | cc | kk) != 0);
           }
           mma_commit(&bars->k_empty[ks]);
-          if (qslot >= 0) mma_commit(&bars->k_empty[qslot]);
+          if (qs >= 0) mma_commit(&bars->k_empty[qs]);
         }
         mma_commit(&bars->s_full);
         return true;
@@ -273,22 +358,43 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = 0; j < nblk && ok; ++j) {
         if (j + 1 < nblk) {
           if (!mbar_wait(&bars->s_free, j & 1, abortf, limit)) { ok = false; break; }
+          TC_TRACE_EV(8, j);
           tc_fence_after();
           if (!issue_s()) { ok = false; break; }
+          TC_TRACE_EV(9, j);
         }
         if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abortf, limit)) { ok = false; break; }
-        const int vs = vctr % prm.vst;
-        if (!mbar_wait(&bars->v_full[vs], (vctr / prm.vst) & 1, abortf, limit)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t vaddr = sv_addr + vs * (prm.vmax * CHUNK_BYTES);
-        const uint32_t pcol = (j & 1) ? TM_P1 : TM_P0;
+        TC_TRACE_EV(10, j);
+        const uint32_t pcol = tmem + ((j & 1) ? TM_P1 : TM_P0);
+        if (prm.vring) {
+          // V_j as ring items of two chunks: O columns [128 v, 128 v + 64 cn)
+          for (int v = 0; v < prm.nvitems; ++v) {
+            int vs;
+            if (!next_item(vs)) { ok = false; break; }
+            tc_fence_after();
+            const int cn = min(2, s_chunks - 2 * v);
+            const uint32_t idesc_v = idesc_bf16(BM, 64 * cn, 0, 1);
+            const uint64_t vd = vd_ring + (uint64_t)vs * kSlotD;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + TM_O, tmem + pcol + kk * 8, smem_desc(vaddr + kk * 2048, CHUNK_BYTES, 1024), idesc_pv,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->v_empty[vs]);
-        ++vctr;
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(tmem + TM_O + 128 * v, pcol + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), idesc_v,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars->k_empty[vs]);
+          }
+          if (!ok) break;
+        } else {
+          const int vs = vctr % prm.vst;
+          if (!mbar_wait(&bars->v_full[vs], (vctr / prm.vst) & 1, abortf, limit)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t vd = vd_sep + (uint64_t)vs * (uint64_t)(prm.vmax * kChunkD);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + TM_O, pcol + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->v_empty[vs]);
+          ++vctr;
+        }
         mma_commit(&bars->o_bar[j & 1]);
+        TC_TRACE_EV(11, j);
       }
       if (!ok) raise_abort(bars, p.status);
       // every MMA this thread issued completes before TMEM is released
@@ -308,6 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int j = 0; j < nblk; ++j) {
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, abortf, limit))) { ok = false; break; }
+      if (tid == 0) TC_TRACE_EV(12, j);
       tc_fence_after();
       uint32_t sr[BN / 32][32];
 #pragma unroll
@@ -384,6 +491,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[j & 1]);
+      if (tid == 0) TC_TRACE_EV(13, j);
     }
 
     if (!ok) raise_abort(bars, p.status);
@@ -446,6 +554,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- teardown
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) TC_TRACE_EV(14, 0);
   if (warp == WARP_MMA) {
     __syncwarp();
     tc_fence_after();
@@ -470,11 +579,18 @@ TcConfig tc_config(int D) {
   // slot (two V slots if three Q/K slots still fit); else Q streams through
   // the ring next to K, with two V slots when four ring slots remain
   c.qres = 0;
+  c.vring = 0;
   c.vst = 1;
   if (qb + vb + 3 * SLOT_BYTES <= avail) {
     c.qres = 1;
     c.vst = (qb + 2 * vb + 3 * SLOT_BYTES <= avail) ? 2 : 1;
     c.kst = (avail - qb - c.vst * vb) / SLOT_BYTES;
+  } else if (qb + 3 * SLOT_BYTES <= avail) {
+    // Q stays resident; V blocks take ring slots between the K pairs
+    c.qres = 1;
+    c.vring = 1;
+    c.vst = 0;
+    c.kst = (avail - qb) / SLOT_BYTES;
   } else {
     c.vst = (2 * vb + 4 * SLOT_BYTES <= avail) ? 2 : 1;
     c.kst = (avail - c.vst * vb) / SLOT_BYTES;
@@ -495,7 +611,7 @@ cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cuda
   CUtensorMap tq, tk, tv;
   if (!make_chunk_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq, BM, c.qres ? c.nc : 2)) return cudaErrorInvalidValue;
   if (!make_chunk_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv, BN, 2)) return cudaErrorInvalidValue;
-  if (!make_chunk_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv, BN, c.vmax)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv, BN, c.vring ? 2 : c.vmax)) return cudaErrorInvalidValue;
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.p = p;
@@ -505,6 +621,8 @@ cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cuda
   prm.kst = c.kst;
   prm.vst = c.vst;
   prm.qres = c.qres;
+  prm.vring = c.vring;
+  prm.nvitems = (c.vmax + 1) / 2;
   prm.vmax = c.vmax;
   prm.npairs = (c.nc + 1) / 2;
   prm.off_q = c.off_q;
