@@ -287,47 +287,57 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0 && nblk > 0) {
       const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
-      const uint32_t sq_addr = smem_u32(sq), sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
       bool ok = MMA_WAIT(&bars->q_full, 0, abortf, limit);
       ATTN_TRACE_EV(25, 0);
-      // S_t,blk = Q_t K_blk^T.  K block blk sits in ring slot blk % kst; Q tile t
-      // chunk c at sq + c*32 KB + t*16 KB (one 256-row copy per chunk).
-      auto issue_s = [&](int t, int blk, bool wait_full, bool release) -> bool {
-        const int s = blk % prm.kst;
-        if (wait_full && !MMA_WAIT(&bars->k_full[s], (blk / prm.kst) & 1, abortf, limit)) return false;
-        if (wait_full) ATTN_TRACE_EV(12, blk);
+      // Descriptors of K-major 128B-swizzled chunks (a K=16 step adds 32 bytes,
+      // 2 in the >>4 address field): Q tile t chunk c at sq + c*32 KB + t*16 KB
+      // (one 256-row copy per chunk); K block in ring slot s at sk + s*NC*16 KB.
+      // V (MN-major): a K=16 step is 16 keys, 2048 bytes.
+      constexpr uint64_t kChunkD = CHUNK_BYTES >> 4, kBlkD = (uint64_t)(NC * CHUNK_BYTES) >> 4;
+      const uint64_t qd_base = smem_desc(smem_u32(sq), 16, 1024);
+      const uint64_t kd_base = smem_desc(smem_u32(sk), 16, 1024);
+      const uint64_t vd_base = smem_desc(smem_u32(sv), CHUNK_BYTES, 1024);
+      // ring positions (slot, phase) of the next K block and of V block j
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
+      // S_t = Q_t K^T for the K block at the current ring position
+      auto issue_s = [&](int t, bool wait_full, bool release) -> bool {
+        if (wait_full && !MMA_WAIT(&bars->k_full[ks], kph, abortf, limit)) return false;
+        if (wait_full) ATTN_TRACE_EV(12, 0);
         tc_fence_after();
-        // descriptor of a K-major 128B-swizzled chunk; the K=16 step inside a
-        // chunk advances its start address by 32 bytes (2 in the >>4 field)
-        const uint64_t qd0 = smem_desc(sq_addr + t * CHUNK_BYTES, 16, 1024);
-        const uint64_t kd0 = smem_desc(sk_addr + s * NC * CHUNK_BYTES, 16, 1024);
+        const uint64_t qd0 = qd_base + (uint64_t)t * kChunkD, kd0 = kd_base + (uint64_t)ks * kBlkD;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + 128 * t, qd0 + (uint64_t)(c * (2 * CHUNK_BYTES >> 4) + kk * 2),
-                   kd0 + (uint64_t)(c * (CHUNK_BYTES >> 4) + kk * 2), idesc_s, (c | kk) != 0);
+            mma_ss(tmem + 128 * t, qd0 + (uint64_t)(c * 2 * kChunkD + kk * 2), kd0 + (uint64_t)(c * kChunkD + kk * 2),
+                   idesc_s, (c | kk) != 0);
         }
-        if (release) mma_commit(&bars->k_empty[s]);
+        if (release) mma_commit(&bars->k_empty[ks]);
         mma_commit(&bars->s_full[t]);
         return true;
       };
+      auto next_k = [&]() {
+        if (++ks == prm.kst) {
+          ks = 0;
+          kph ^= 1u;
+        }
+      };
       auto act = [&](int t, int j) { return j < nblk_t[t]; };
-      if (ok && act(0, 0)) ok = issue_s(0, 0, true, !act(1, 0));
-      if (ok && act(1, 0)) ok = issue_s(1, 0, !act(0, 0), true);
+      if (ok && act(0, 0)) ok = issue_s(0, true, !act(1, 0));
+      if (ok && act(1, 0)) ok = issue_s(1, !act(0, 0), true);
+      next_k();
       for (int j = 0; j < nblk && ok; ++j) {
-        const int vs = j % prm.vst;
         ATTN_TRACE_EV(10, j);
-        if (!MMA_WAIT(&bars->v_full[vs], (j / prm.vst) & 1, abortf, limit)) { ok = false; break; }
+        if (!MMA_WAIT(&bars->v_full[vs], vph, abortf, limit)) { ok = false; break; }
         ATTN_TRACE_EV(11, j);
-        const uint32_t vaddr = sv_addr + vs * NC * CHUNK_BYTES;
+        const uint64_t vd0 = vd_base + (uint64_t)vs * kBlkD;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!act(t, j)) continue;
           if (!MMA_WAIT(&bars->p_full[t], j & 1, abortf, limit)) { ok = false; break; }
           ATTN_TRACE_EV(8 + t, j);
           tc_fence_after();
-          const uint64_t vd0 = smem_desc(vaddr, CHUNK_BYTES, 1024);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, vd0 + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
@@ -337,12 +347,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (act(t, j + 1)) {
             const bool first = (t == 0) || !act(0, j + 1);
             const bool last = (t == 1) || !act(1, j + 1);
-            if (!issue_s(t, j + 1, first, last)) { ok = false; break; }
+            if (!issue_s(t, first, last)) { ok = false; break; }
           }
           if (t == 0) ATTN_TRACE_EV(15, j);
         }
         if (!ok) break;
         mma_commit(&bars->v_empty[vs]);
+        next_k();
+        if (++vs == prm.vst) {
+          vs = 0;
+          vph ^= 1u;
+        }
       }
       if (!ok) raise_abort(bars, p.status);
       mma_commit(&bars->done);
