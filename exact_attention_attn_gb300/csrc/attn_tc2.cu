@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t *sq = smem;  // Q0 chunks then Q1 chunks
+  uint8_t *sq = smem;  // Q tile t: its NC chunks at t*NC*16 KB + c*16 KB
   uint8_t *sk = smem + prm.off_k;
   uint8_t *sv = smem + prm.off_v;
   Bars2 *bars = reinterpret_cast<Bars2 *>(smem + prm.off_bar);
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nblk = je - jb;
 
   if (tid == 0) {
-    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_full, 2);  // one Q tile from each producer
     for (int i = 0; i < prm.kst; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -227,38 +227,50 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == WARP_LOAD_K || warp == WARP_LOAD_V) {
     // ------------------------------------------------------------ producers
-    // Two independent producer threads (Q+K and V), each moving a whole
-    // 128-key block (all D/64 chunks) with one 4-D TMA copy.
+    // Two independent producer threads (Q0+K and Q1+V), each moving a whole
+    // 128-row tile or 128-key block (all D/64 chunks) with one 4-D TMA copy:
+    // copies issued by one thread are processed one after the other, so the
+    // two query tiles travel in parallel.
     if (lane == 0 && nblk > 0) {
       const bool is_k = warp == WARP_LOAD_K;
       uint32_t ctr = 0;
+      int slot = 0;
+      uint32_t phase = 0;
       uint32_t skipped = 0xffffffffu;  // a copy never issued (test support)
       bool ok = true;
+      tma_prefetch_desc(&tm_q);
+      // query tile 0 (K producer) or 1 (V producer), zero-filled past Nq
+      const int qt = is_k ? 0 : 1;
+      mbar_arrive_expect_tx(&bars->q_full, NC * CHUNK_BYTES);
+      tma_load_4d(sq + qt * NC * CHUNK_BYTES, &tm_q, &bars->q_full, 0, pair * 2 * BM + qt * BM, 0, bh);
       if (is_k) {
-        tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
-        // both query tiles (256 rows, zero-filled past Nq) in one copy
-        mbar_arrive_expect_tx(&bars->q_full, 2 * NC * CHUNK_BYTES);
-        tma_load_4d(sq, &tm_q, &bars->q_full, 0, pair * 2 * BM, 0, bh);
         // warm L2 with the first blocks; later ones are prefetched kPrefetch
         // blocks ahead of their shared-memory copy
         for (int j = 0; j < kPrefetch && j < nblk; ++j) tma_prefetch_4d(&tm_k, 0, (jb + j) * BN, 0, bkv);
         for (int j = 0; j < nblk; ++j) {
           if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_k, 0, (jb + j + kPrefetch) * BN, 0, bkv);
-          const int s = ctr % prm.kst;
-          if (!mbar_wait(&bars->k_empty[s], ((ctr / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->k_full[s], NC * CHUNK_BYTES);
-          tma_load_4d(sk + s * NC * CHUNK_BYTES, &tm_k, &bars->k_full[s], 0, (jb + j) * BN, 0, bkv);
+          if (!mbar_wait(&bars->k_empty[slot], phase ^ 1u, abortf, limit)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->k_full[slot], NC * CHUNK_BYTES);
+          tma_load_4d(sk + slot * NC * CHUNK_BYTES, &tm_k, &bars->k_full[slot], 0, (jb + j) * BN, 0, bkv);
           ATTN_TRACE_EV(13, j);
           ++ctr;
+          if (++slot == prm.kst) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
       } else {
         tma_prefetch_desc(&tm_v);
         for (int j = 0; j < kPrefetch && j < nblk; ++j) tma_prefetch_4d(&tm_v, 0, (jb + j) * BN, 0, bkv);
         for (int j = 0; j < nblk; ++j) {
           if (j + kPrefetch < nblk) tma_prefetch_4d(&tm_v, 0, (jb + j + kPrefetch) * BN, 0, bkv);
-          const int vs = ctr % prm.vst;
-          if (!mbar_wait(&bars->v_empty[vs], ((ctr / prm.vst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+          const int vs = slot;
+          if (!mbar_wait(&bars->v_empty[vs], phase ^ 1u, abortf, limit)) { ok = false; break; }
+          if (++slot == prm.vst) {
+            slot = 0;
+            phase ^= 1u;
+          }
           if ((p.debug_flags & 1) && j == 1) {  // test support: leave this slot empty
             skipped = ctr;
             ++ctr;
@@ -272,8 +284,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) raise_abort(bars, p.status);
       // drain: every copy this thread issued lands before the CTA exits
+      mbar_wait_drain(&bars->q_full, 0, limit);
       if (is_k) {
-        mbar_wait_drain(&bars->q_full, 0, limit);
         const uint32_t kn = ctr < (uint32_t)prm.kst ? ctr : (uint32_t)prm.kst;
         for (uint32_t i = ctr - kn; i < ctr; ++i) mbar_wait_drain(&bars->k_full[i % prm.kst], (i / prm.kst) & 1, limit);
       } else {
@@ -290,8 +302,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = MMA_WAIT(&bars->q_full, 0, abortf, limit);
       ATTN_TRACE_EV(25, 0);
       // Descriptors of K-major 128B-swizzled chunks (a K=16 step adds 32 bytes,
-      // 2 in the >>4 address field): Q tile t chunk c at sq + c*32 KB + t*16 KB
-      // (one 256-row copy per chunk); K block in ring slot s at sk + s*NC*16 KB.
+      // 2 in the >>4 address field): Q tile t chunk c at sq + (t*NC + c)*16 KB;
+      // K block in ring slot s at sk + s*NC*16 KB.
       // V (MN-major): a K=16 step is 16 keys, 2048 bytes.
       constexpr uint64_t kChunkD = CHUNK_BYTES >> 4, kBlkD = (uint64_t)(NC * CHUNK_BYTES) >> 4;
       const uint64_t qd_base = smem_desc(smem_u32(sq), 16, 1024);
@@ -305,12 +317,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (wait_full && !MMA_WAIT(&bars->k_full[ks], kph, abortf, limit)) return false;
         if (wait_full) ATTN_TRACE_EV(12, 0);
         tc_fence_after();
-        const uint64_t qd0 = qd_base + (uint64_t)t * kChunkD, kd0 = kd_base + (uint64_t)ks * kBlkD;
+        const uint64_t qd0 = qd_base + (uint64_t)t * kBlkD, kd0 = kd_base + (uint64_t)ks * kBlkD;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + 128 * t, qd0 + (uint64_t)(c * 2 * kChunkD + kk * 2), kd0 + (uint64_t)(c * kChunkD + kk * 2),
+            mma_ss(tmem + 128 * t, qd0 + (uint64_t)(c * kChunkD + kk * 2), kd0 + (uint64_t)(c * kChunkD + kk * 2),
                    idesc_s, (c | kk) != 0);
         }
         if (release) mma_commit(&bars->k_empty[ks]);
@@ -558,7 +570,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // its last reader, S_t of the last block, completed before o_done) in
         // the 128B-swizzled layout of a 128-row TMA box, 16-byte unit u of
         // row r at r*128 + ((u ^ (r % 8)) * 16) of each 64-column chunk
-        const uint32_t stage = smem_u32(sq) + t * CHUNK_BYTES + row * 128;
+        const uint32_t stage = smem_u32(sq) + t * NC * CHUNK_BYTES + row * 128;
         // a tile without keys gets here at once: the pair's Q copy (issued
         // whenever the CTA has a block) must land before its region is reused
         bool staged_ok = true;
@@ -575,7 +587,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
           }
-          const uint32_t chunk = stage + (cc >> 1) * 2 * CHUNK_BYTES;
+          const uint32_t chunk = stage + (cc >> 1) * CHUNK_BYTES;
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
             const uint32_t u = (cc & 1) * 4 + v4;
@@ -622,7 +634,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (row == 0 && q0 < p.Nq) {
         if (mbar_wait(&bars->o_staged[t], 0, abortf, limit)) {
 #pragma unroll
-          for (int c = 0; c < NC; ++c) tma_store_4d(&tm_o, sq + c * 2 * CHUNK_BYTES + t * CHUNK_BYTES, 0, q0, c, bh);
+          tma_store_4d(&tm_o, sq + t * NC * CHUNK_BYTES, 0, q0, 0, bh);
           bulk_commit_group();
           bulk_wait_group_read0();
         } else if (!*abortf) {
@@ -677,10 +689,9 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
   const int smem = prm.off_bar + (int)sizeof(Bars2) + 1024;
   if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv, to;
-  if (!make_block_map(&tq, p.q, D, p.Nq, p.B * p.Hq, 2 * BM)) return cudaErrorInvalidValue;
-  // O: one 64-column chunk of a 128-row tile per store (the staging chunks of a
-  // tile are 32 KB apart); unused by split-KV launches, whose output is fp32
-  if (!make_chunk_map(&to, p.o, D, p.Nq, p.B * p.Hq, BM, 1)) return cudaErrorInvalidValue;
+  if (!make_block_map(&tq, p.q, D, p.Nq, p.B * p.Hq, BM)) return cudaErrorInvalidValue;
+  // O: a whole 128-row tile per store; unused by split-KV launches (fp32 output)
+  if (!make_block_map(&to, p.o, D, p.Nq, p.B * p.Hq, BM)) return cudaErrorInvalidValue;
   if (!make_block_map(&tk, p.k, D, p.Nkv, p.B * p.Hkv, BN)) return cudaErrorInvalidValue;
   if (!make_block_map(&tv, p.v, D, p.Nkv, p.B * p.Hkv, BN)) return cudaErrorInvalidValue;
   static std::atomic<int> attr_set[64];
