@@ -339,9 +339,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ok && act(0, 0)) ok = issue_s(0, true, !act(1, 0));
       if (ok && act(1, 0)) ok = issue_s(1, !act(0, 0), true);
       next_k();
+      // from block 0 on, V_j and K_{j+1} have landed once P of the block's first
+      // tile is complete (a softmax thread of that tile waits for both before it
+      // arrives), so this thread waits only for P
       for (int j = 0; j < nblk && ok; ++j) {
         ATTN_TRACE_EV(10, j);
-        if (!MMA_WAIT(&bars->v_full[vs], vph, abortf, limit)) { ok = false; break; }
         ATTN_TRACE_EV(11, j);
         const uint64_t vd0 = vd_base + (uint64_t)vs * kBlkD;
 #pragma unroll
@@ -357,9 +359,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (t == 0) ATTN_TRACE_EV(18, j);
           if (j == nblk_t[t] - 1) mma_commit(&bars->o_done[t]);
           if (act(t, j + 1)) {
-            const bool first = (t == 0) || !act(0, j + 1);
             const bool last = (t == 1) || !act(1, j + 1);
-            if (!issue_s(t, first, last)) { ok = false; break; }
+            if (!issue_s(t, false, last)) { ok = false; break; }
           }
           if (t == 0) ATTN_TRACE_EV(15, j);
         }
@@ -404,6 +405,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const Exp2Poly exp2_poly;
 
     const bool tr = (tid & 127) == 0;
+    // ring positions of V_j and K_{j+1}, followed by thread 0 of the tile in one
+    // register: V slot bits 0-7, K slot bits 8-15, V phase bit 16, K phase bit 24
+    uint32_t ring = 1u << 8;
     for (int j = 0; j < nb; ++j) {
       if (tr) ATTN_TRACE_EV(4 * t + 0, j);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abortf, limit))) { ok = false; break; }
@@ -547,6 +551,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
+      // the block's first tile (tile 0, or tile 1 where tile 0 has no keys in
+      // this block) vouches for V_j and K_{j+1}: the MMA thread then needs to
+      // wait for P alone
+      if (row == 0 && (t == 0 || j >= nblk_t[0])) {
+        bool got = mbar_wait(&bars->v_full[ring & 0xffu], (ring >> 16) & 1u, abortf, limit);
+        if (got && j + 1 < nblk) got = mbar_wait(&bars->k_full[(ring >> 8) & 0xffu], ring >> 24, abortf, limit);
+        if (!got) raise_abort(bars, p.status);  // every role stops waiting
+      }
+      if (row == 0) {
+        ring += 1u;
+        if ((ring & 0xffu) == (uint32_t)prm.vst) ring = (ring & ~0xffu) ^ (1u << 16);
+        ring += 1u << 8;
+        if (((ring >> 8) & 0xffu) == (uint32_t)prm.kst) ring = (ring & ~0xff00u) ^ (1u << 24);
+      }
       mbar_arrive(&bars->p_full[t]);
       if (tr) ATTN_TRACE_EV(4 * t + 3, j);
     }
@@ -633,7 +651,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int q0 = pair * 2 * BM + t * BM;
       if (row == 0 && q0 < p.Nq) {
         if (mbar_wait(&bars->o_staged[t], 0, abortf, limit)) {
-#pragma unroll
           tma_store_4d(&tm_o, sq + t * NC * CHUNK_BYTES, 0, q0, 0, bh);
           bulk_commit_group();
           bulk_wait_group_read0();
