@@ -129,7 +129,6 @@ struct Bars2 {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
-  uint64_t o_staged[2];  // tile t's rows of O are in shared memory (count 128)
   uint64_t done;
   uint32_t tmem_slot;
   int abort;
@@ -143,8 +142,7 @@ __device__ __forceinline__ void raise_abort(Bars2 *bars, int *status) {
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const Params2 prm) {
+                    const __grid_constant__ CUtensorMap tm_v, const Params2 prm) {
   constexpr int NC = D / 64;  // 64-column chunks per row
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -210,7 +208,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 128);
       mbar_init(&bars->o_done[t], 1);
-      mbar_init(&bars->o_staged[t], 128);
     }
     mbar_init(&bars->done, 1);
     bars->abort = 0;
@@ -584,18 +581,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float lse_val = (m_use == -INFINITY || !(l > 0.f)) ? -INFINITY : (m_use + log2f(l)) * kLn2;
       const int64_t row_idx = (int64_t)bh * p.Nq + qi;
       if (nsplit == 1) {
-        // O_t normalised and rounded to bf16 goes to this tile's Q region (free:
-        // its last reader, S_t of the last block, completed before o_done) in
-        // the 128B-swizzled layout of a 128-row TMA box, 16-byte unit u of
-        // row r at r*128 + ((u ^ (r % 8)) * 16) of each 64-column chunk
-        const uint32_t stage = smem_u32(sq) + t * NC * CHUNK_BYTES + row * 128;
-        // a tile without keys gets here at once: the pair's Q copy (issued
-        // whenever the CTA has a block) must land before its region is reused
-        bool staged_ok = true;
-        if (nb == 0 && nblk > 0) staged_ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abortf, limit));
-        if (!staged_ok) raise_abort(bars, p.status);
+        __nv_bfloat16 *orow = p.o + row_idx * D;
 #pragma unroll
-        for (int cc = 0; cc < D / 32 && staged_ok; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t r[32];
           if (nb > 0) {
             tmem_ld32(tO + cc * 32, r);
@@ -605,15 +593,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
           }
-          const uint32_t chunk = stage + (cc >> 1) * CHUNK_BYTES;
+          if (qi < p.Nq) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const uint32_t u = (cc & 1) * 4 + v4;
-            st_shared_v4(chunk + ((u ^ (row & 7)) << 4),
-                         pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv),
-                         pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv),
-                         pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv),
-                         pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv));
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
+              dst[v4] = w;
+            }
           }
         }
         if (qi < p.Nq) p.lse[row_idx] = lse_val;
@@ -641,22 +631,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         if (qi < p.Nq) p.ws_lse[ws_row] = lse_val;
-      }
-    }
-    if (nsplit == 1) {
-      // every thread of the tile arrives, staged or not; one thread stores the
-      // tile (rows past Nq are clipped by the tensor map) unless the CTA aborted
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->o_staged[t]);
-      const int q0 = pair * 2 * BM + t * BM;
-      if (row == 0 && q0 < p.Nq) {
-        if (mbar_wait(&bars->o_staged[t], 0, abortf, limit)) {
-          tma_store_4d(&tm_o, sq + t * NC * CHUNK_BYTES, 0, q0, 0, bh);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-        } else if (!*abortf) {
-          raise_abort(bars, p.status);
-        }
       }
     }
   }
@@ -705,10 +679,8 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
   prm.wait_limit_ns = wait_limit_ns;
   const int smem = prm.off_bar + (int)sizeof(Bars2) + 1024;
   if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   if (!make_block_map(&tq, p.q, D, p.Nq, p.B * p.Hq, BM)) return cudaErrorInvalidValue;
-  // O: a whole 128-row tile per store; unused by split-KV launches (fp32 output)
-  if (!make_block_map(&to, p.o, D, p.Nq, p.B * p.Hq, BM)) return cudaErrorInvalidValue;
   if (!make_block_map(&tk, p.k, D, p.Nkv, p.B * p.Hkv, BN)) return cudaErrorInvalidValue;
   if (!make_block_map(&tv, p.v, D, p.Nkv, p.B * p.Hkv, BN)) return cudaErrorInvalidValue;
   static std::atomic<int> attr_set[64];
@@ -720,7 +692,7 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
   }
   const int64_t grid = (int64_t)prm.npairs * p.B * p.Hq * p.kv_splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  attn_tc2_kernel<D><<<(unsigned)grid, THREADS, smem, stream>>>(tq, tk, tv, to, prm);
+  attn_tc2_kernel<D><<<(unsigned)grid, THREADS, smem, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError();
 }
 
