@@ -61,6 +61,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_splitkv.restype = ci
         lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
         lib.attn_fwd_splitkv_noalloc.restype = ci
+        lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+        lib.attn_fwd_host.restype = ci
         lib.attn_set_debug.argtypes = [ci, ctypes.c_longlong]
         lib.attn_set_debug.restype = ci
         lib.attn_fwd_status.argtypes = [vp]
@@ -147,25 +149,47 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | N
     return out, lse
 
 
+def _check_host(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
 def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
                   causal: bool = False, device=None, out: torch.Tensor | None = None,
-                  lse: torch.Tensor | None = None):
-    """Host-buffer form of attn_fwd: copies q, k, v (CPU, ideally pinned) to
-    the device, runs the kernel, copies O and LSE back into host tensors and
-    waits for them.  Returns (O, LSE) on the CPU."""
-    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    stream = torch.cuda.current_stream(dev)
-    dq = q.to(dev, non_blocking=True)
-    dk = k.to(dev, non_blocking=True)
-    dv = v.to(dev, non_blocking=True)
-    do, dl = attn_fwd(dq, dk, dv, scale=scale, causal=causal, stream=stream)
+                  lse: torch.Tensor | None = None, stream=None):
+    """attn_fwd_host of the C ABI: q, k, v, out and lse are CPU tensors (pin
+    them for the copies to overlap the kernels); runs on ``device`` (default:
+    the current CUDA device) and returns (O, LSE) on the CPU once they are there."""
+    lib = load_library()
+    _check_host(q, "q", torch.bfloat16, 4)
+    _check_host(k, "k", torch.bfloat16, 4)
+    _check_host(v, "v", torch.bfloat16, 4)
+    B, Hq, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError(f"k {tuple(k.shape)} / v {tuple(v.shape)} do not match q {tuple(q.shape)}")
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty(do.shape, dtype=do.dtype, pin_memory=True)
+        out = torch.empty((B, Hq, Nq, D), dtype=torch.bfloat16, pin_memory=q.is_pinned())
     if lse is None:
-        lse = torch.empty(dl.shape, dtype=dl.dtype, pin_memory=True)
-    out.copy_(do, non_blocking=True)
-    lse.copy_(dl, non_blocking=True)
-    stream.synchronize()
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=q.is_pinned())
+    _check_host(out, "out", torch.bfloat16, 4)
+    _check_host(lse, "lse", torch.float32, 3)
+    if tuple(out.shape) != (B, Hq, Nq, D) or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("out / lse shape mismatch")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        rc = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, Hq, Hkv, Nq, Nkv, D, float(scale), int(bool(causal)), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
     return out, lse
 
 

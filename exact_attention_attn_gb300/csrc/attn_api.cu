@@ -198,6 +198,10 @@ int current_device(int *device, int *sm_count, int **status) {
 
 int record_cuda_error(cudaError_t e) { return record(e); }
 
+int check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal) {
+  return check_sizes(B, Hq, Hkv, Nq, Nkv, D, causal);
+}
+
 uint64_t wait_limit_ns() { return (uint64_t)g_wait_limit_ns.load(std::memory_order_relaxed); }
 int debug_flags() { return g_debug_flags.load(std::memory_order_relaxed); }
 

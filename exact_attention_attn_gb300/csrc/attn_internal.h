@@ -84,6 +84,8 @@ int debug_flags();
 int current_device(int *device, int *sm_count, int **status);
 // Records a CUDA error for attn_last_cuda_error; returns ATTN_ERR_LAUNCH.
 int record_cuda_error(cudaError_t e);
+// The size and flag checks of attn_fwd (ATTN_OK or ATTN_ERR_ARG), no device work.
+int check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal);
 
 // Plain CUDA-core kernel: correct for every supported shape; used for the
 // shapes the tensor-core kernel does not take.

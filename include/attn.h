@@ -116,6 +116,40 @@ ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, void 
                               float scale, int causal, int kv_splits, attn_stream_t stream);
 
 /*
+ * attn_fwd_host -- attn_fwd on host buffers.
+ *
+ * q, k, v, o and lse are HOST pointers with the layouts of attn_fwd
+ * (contiguous [B, H, N, D] bf16, lse [B, Hq, Nq] fp32; no alignment needed).
+ * The call copies the inputs to the current device, runs the same kernels as
+ * attn_fwd (the same key split count, so O and LSE are bit-identical to
+ * attn_fwd's), copies O and LSE back and returns when they are in host
+ * memory: the caller may reuse every buffer at once.
+ *
+ * The work is cut by (b, kv head) group -- independent attention problems
+ * whose rows are contiguous -- into up to four chunks; a chunk's inputs go up
+ * on a copy stream of the library's, its kernels run on `stream` as soon as
+ * they have landed, and its outputs come down on a second copy stream, so that
+ * the copies of one chunk overlap the kernels and the copies of the others.
+ * The copies overlap only when the host buffers are page-locked
+ * (cudaHostAlloc / cudaHostRegister); with pageable memory the call is still
+ * correct but the copies run one after the other.
+ *
+ * Device memory: one stream-ordered block on `stream` for the device copies
+ * of all five tensors (plus what attn_fwd itself may take for key splits),
+ * freed before the call returns into a memory pool of the library's that keeps
+ * it for the next call (a device holds up to the largest block asked for).  The two copy streams are created on a
+ * device's first call and reused; calls on the same device serialise on them
+ * (the call is synchronous anyway).  Errors: those of attn_fwd, plus
+ * ATTN_ERR_NOMEM when the device block cannot be allocated.
+ *
+ * The pages describe no host-buffer entry point; this one exists so that the
+ * library can be measured, and used, end to end from host memory.
+ */
+ATTN_API int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                           float scale, int causal, attn_stream_t stream);
+
+/*
  * attn_fwd_splitkv_noalloc -- attn_fwd_splitkv that allocates nothing.
  *
  * The pages have no counterpart of this call; it exists for callers that may

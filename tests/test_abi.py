@@ -98,6 +98,22 @@ def test_splitkv_argument_errors(lib):
     assert lib.attn_fwd_splitkv(None, None, None, None, None, 0, 2, 1, 8, 8, 64, 0.125, 0, 2, None) == 0
 
 
+def test_host_entry_argument_errors(lib):
+    import ctypes as C
+    lib.attn_fwd_host.argtypes = [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_float, C.c_int, C.c_void_p]
+    b = Buf()
+    p = b.p
+    # sizes, flags, scale and pointers are checked on the host before any device work
+    assert lib.attn_fwd_host(p, p, p, p, p, 1, 2, 1, 8, 8, 65, 0.125, 0, None) == -1
+    assert lib.attn_fwd_host(p, p, p, p, p, 1, 3, 2, 8, 8, 64, 0.125, 0, None) == -1
+    assert lib.attn_fwd_host(p, p, p, p, p, 1, 2, 1, 8, 8, 64, float("nan"), 0, None) == -1
+    assert lib.attn_fwd_host(p, p, p, p, p, 1, 2, 1, 8, 8, 64, 0.125, 3, None) == -1
+    assert lib.attn_fwd_host(None, p, p, p, p, 1, 2, 1, 8, 8, 64, 0.125, 0, None) == -1
+    assert lib.attn_fwd_host(p, p, p, p, None, 1, 2, 1, 8, 8, 64, 0.125, 0, None) == -1
+    # host buffers need no alignment: a misaligned pointer fails only on the device side, not here
+    assert lib.attn_fwd_host(None, None, None, None, None, 0, 2, 1, 8, 8, 64, 0.125, 0, None) == 0
+
+
 def test_set_debug_arguments(lib):
     lib.attn_set_debug.argtypes = [ctypes.c_int, ctypes.c_longlong]
     assert lib.attn_set_debug(2, 0) == -1
