@@ -139,7 +139,9 @@ __device__ __forceinline__ void raise_abort(Bars2 *bars, int *status) {
   *reinterpret_cast<volatile int *>(&bars->abort) = 1;
 }
 
-template <int D>
+// POS: the scale is positive (scores and their maxima keep their order); the
+// other sign takes minima and needs no separate fast path
+template <int D, bool POS>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params2 prm) {
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int nb = nblk_t[t];
     const int vis_end = p.causal ? min(p.Nkv, qi + shift + 1) : p.Nkv;
     const float sl2 = p.scale * kLog2e;
-    const bool pos = sl2 > 0.f;  // uniform across the CTA
+    constexpr bool pos = POS;  // sl2 > 0, decided by the host
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
     const Exp2Poly exp2_poly;
@@ -473,7 +475,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float mu = (m_use == -INFINITY) ? 0.f : m_use;
       // the branch must be warp-uniform: both sides end in the warp-collective
       // tcgen05.st, which every lane of the warp has to execute together
-      if (__all_sync(0xffffffffu, pos && full)) {
+      if (pos && __all_sync(0xffffffffu, full)) {
         // every key visible and scale > 0: y = s*sl2 - mu on f32x2 pairs,
         // exp2 on the MUFU (pairs selected by kPolyPairs on the FMA pipe)
         // The scores are read again from TMEM a quarter at a time (the next
@@ -523,22 +525,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         f2_unpack(acc1, b0, b1);
         l += (a0 + a1) + (b0 + b1);
       } else {
+        // a block with masked keys (or scale <= 0): the scores are read again a
+        // quarter at a time as above, and a masked key gives exactly 0.  One
+        // quarter's code, looped: unrolling it measured 3 % slower overall
+        // (this kernel is sensitive to the size of its code)
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
         for (int h = 0; h < 4; ++h) {
+          uint32_t cur[32];
+          tmem_ld32(tS + 32 * h, cur);
+          tmem_wait_ld();
+          reg_fence32(cur);
+          const int c0 = kbase + 32 * h;
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a = x[h * 32 + 2 * i], bb = x[h * 32 + 2 * i + 1];
-            // masked entries hold -inf (or +inf when scale < 0) and give exactly 0
-            float p0, p1;
-            if (pos) {
-              p0 = ex2_approx(fmaf(a, sl2, -mu));
-              p1 = ex2_approx(fmaf(bb, sl2, -mu));
-            } else {
-              p0 = (a == INFINITY) ? 0.f : ex2_approx(fmaf(a, sl2, -mu));
-              p1 = (bb == INFINITY) ? 0.f : ex2_approx(fmaf(bb, sl2, -mu));
-            }
+            const float a = __uint_as_float(cur[2 * i]), bb = __uint_as_float(cur[2 * i + 1]);
+            const float p0 = (c0 + 2 * i >= vis_end) ? 0.f : ex2_approx(fmaf(a, sl2, -mu));
+            const float p1 = (c0 + 2 * i + 1 >= vis_end) ? 0.f : ex2_approx(fmaf(bb, sl2, -mu));
             ls[i & 3] += p0 + p1;
             pk[i] = pack_bf16x2(p0, p1);
           }
@@ -647,7 +651,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool POS>
 cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
   constexpr int NC = D / 64;
   const int avail = kSmemMax - 2048;
@@ -686,13 +690,13 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
   static std::atomic<int> attr_set[64];
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[device].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc2_kernel<D, POS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
     attr_set[device].store(1, std::memory_order_release);
   }
   const int64_t grid = (int64_t)prm.npairs * p.B * p.Hq * p.kv_splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  attn_tc2_kernel<D><<<(unsigned)grid, THREADS, smem, stream>>>(tq, tk, tv, prm);
+  attn_tc2_kernel<D, POS><<<(unsigned)grid, THREADS, smem, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError();
 }
 
@@ -701,8 +705,12 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
 bool tc2_supports(int D) { return D == 64 || D == 128; }
 
 cudaError_t launch_tc2(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
-  if (p.D == 64) return launch_tc2_d<64>(p, device, wait_limit_ns, stream);
-  if (p.D == 128) return launch_tc2_d<128>(p, device, wait_limit_ns, stream);
+  // the same product as the kernel's, so that both sides agree on its sign
+  const bool pos = p.scale * kLog2e > 0.f;
+  if (p.D == 64) return pos ? launch_tc2_d<64, true>(p, device, wait_limit_ns, stream)
+                            : launch_tc2_d<64, false>(p, device, wait_limit_ns, stream);
+  if (p.D == 128) return pos ? launch_tc2_d<128, true>(p, device, wait_limit_ns, stream)
+                             : launch_tc2_d<128, false>(p, device, wait_limit_ns, stream);
   return cudaErrorInvalidValue;
 }
 
