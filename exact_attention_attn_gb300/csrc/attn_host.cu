@@ -5,11 +5,13 @@
 // each group's rows are contiguous in the [B, H, N, D] layouts: Q, O and LSE
 // planes g*G .. g*G + G - 1 (G = Hq / Hkv query heads per kv head), K and V
 // plane g.  The groups are cut into a few chunks; chunk c's inputs go up on one
-// copy stream, its kernels run on the caller's stream once they have landed,
-// and its outputs come back on a second copy stream, so that the copies of one
-// chunk overlap the kernels and copies of the others.  Every chunk uses the key
-// split count of the whole problem, and each (b, h) row tile is computed by the
-// same kernel code as in attn_fwd: the results are bit-identical to attn_fwd.
+// copy stream, its kernels run on a compute stream of its own once they have
+// landed, and its outputs come back on a second copy stream, so that the
+// copies of one chunk overlap the kernels and copies of the others, and the
+// kernels of chunks too small to fill the GPU run side by side.  Every chunk
+// uses the key split count of the whole problem, and each (b, h) row tile is
+// computed by the same kernel code as in attn_fwd: the results are
+// bit-identical to attn_fwd.
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -27,6 +29,7 @@ constexpr int kMaxChunks = 4;
 
 struct CopyStreams {
   cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t k[kMaxChunks] = {};  // chunk c's kernels
   // the library's own pool for the device copies: it keeps its memory between
   // calls (the default pool hands it back to the driver at every synchronise,
   // and a 100 MB block from the driver costs more than the copies it serves)
@@ -67,6 +70,9 @@ extern "C" int attn_fwd_host(const void *q, const void *k, const void *v, void *
     return record_cuda_error(e);
   if (!cs.out && (e = cudaStreamCreateWithFlags(&cs.out, cudaStreamNonBlocking)) != cudaSuccess)
     return record_cuda_error(e);
+  for (int c = 0; c < chunks; ++c)
+    if (!cs.k[c] && (e = cudaStreamCreateWithFlags(&cs.k[c], cudaStreamNonBlocking)) != cudaSuccess)
+      return record_cuda_error(e);
   if (!cs.pool) {
     cudaMemPoolProps props;
     memset(&props, 0, sizeof(props));
@@ -126,33 +132,41 @@ extern "C" int attn_fwd_host(const void *q, const void *k, const void *v, void *
       e = cudaMemcpyAsync(buf + off_v + ko, static_cast<const char *>(v) + ko, kn, cudaMemcpyHostToDevice, cs.in);
     if (e == cudaSuccess) e = cudaEventRecord(ev_in[c], cs.in);
   }
-  // kernels and outputs, chunk by chunk
+  // kernels and outputs, chunk by chunk (chunk c's kernels, and the split-KV
+  // workspace they may take, on compute stream c)
+  int launched = 0;
   for (int c = 0; c < chunks && e == cudaSuccess && rc == ATTN_OK; ++c) {
     const int a = g0(c), n = g0(c + 1) - a;
     const size_t qo = (size_t)a * grp * qplane, qn = (size_t)n * grp * qplane;
     const size_t ko = (size_t)a * kvplane, lo = (size_t)a * grp * lplane, ln = (size_t)n * grp * lplane;
     float *dl = reinterpret_cast<float *>(buf + off_l[c]);
-    e = cudaStreamWaitEvent(st, ev_in[c], 0);
+    e = cudaStreamWaitEvent(cs.k[c], ev_in[c], 0);
     if (e != cudaSuccess) break;
+    launched = c + 1;
     rc = attn_fwd_splitkv(buf + qo, buf + off_k + ko, buf + off_v + ko, buf + off_o + qo, dl, 1, n * grp, n, Nq,
-                          Nkv, D, scale, causal, plan.kv_splits, stream);
+                          Nkv, D, scale, causal, plan.kv_splits, reinterpret_cast<attn_stream_t>(cs.k[c]));
     if (rc != ATTN_OK) break;
-    e = cudaEventRecord(ev_k[c], st);
+    e = cudaEventRecord(ev_k[c], cs.k[c]);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev_k[c], 0);
     if (e == cudaSuccess) e = cudaMemcpyAsync(static_cast<char *>(o) + qo, buf + off_o + qo, qn, cudaMemcpyDeviceToHost, cs.out);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(reinterpret_cast<char *>(lse) + lo, dl, ln, cudaMemcpyDeviceToHost, cs.out);
   }
-  // the buffers are freed after every copy on both streams (also when a step
-  // above failed: then, if the streams cannot be ordered by events, by waiting
-  // for them); the call returns when the outputs are in host memory
-  const bool ordered = ev_indone && ev_out && cudaEventRecord(ev_indone, cs.in) == cudaSuccess &&
-                       cudaEventRecord(ev_out, cs.out) == cudaSuccess &&
-                       cudaStreamWaitEvent(st, ev_indone, 0) == cudaSuccess &&
-                       cudaStreamWaitEvent(st, ev_out, 0) == cudaSuccess;
+  // the buffers are freed after every copy and kernel on the library's streams
+  // (also when a step above failed: then, if the streams cannot be ordered by
+  // events, by waiting for them); the call returns when the outputs are in
+  // host memory
+  bool ordered = ev_indone && ev_out && cudaEventRecord(ev_indone, cs.in) == cudaSuccess &&
+                 cudaEventRecord(ev_out, cs.out) == cudaSuccess &&
+                 cudaStreamWaitEvent(st, ev_indone, 0) == cudaSuccess &&
+                 cudaStreamWaitEvent(st, ev_out, 0) == cudaSuccess;
+  for (int c = 0; c < launched && ordered; ++c)
+    ordered = ev_k[c] && cudaEventRecord(ev_k[c], cs.k[c]) == cudaSuccess &&
+              cudaStreamWaitEvent(st, ev_k[c], 0) == cudaSuccess;
   if (!ordered) {
     cudaStreamSynchronize(cs.in);
     cudaStreamSynchronize(cs.out);
+    for (int c = 0; c < launched; ++c) cudaStreamSynchronize(cs.k[c]);
   }
   cudaError_t f = cudaFreeAsync(buf, st);
   const cudaError_t fs = cudaStreamSynchronize(st);

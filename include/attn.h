@@ -127,9 +127,12 @@ ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, void 
  *
  * The work is cut by (b, kv head) group -- independent attention problems
  * whose rows are contiguous -- into up to four chunks; a chunk's inputs go up
- * on a copy stream of the library's, its kernels run on `stream` as soon as
- * they have landed, and its outputs come down on a second copy stream, so that
- * the copies of one chunk overlap the kernels and the copies of the others.
+ * on a copy stream of the library's, its kernels run on a compute stream of
+ * the library's (one per chunk) as soon as they have landed, and its outputs
+ * come down on a second copy stream, so that the copies of one chunk overlap
+ * the kernels and the copies of the others, and chunks too small to fill the
+ * GPU compute side by side.  The work starts after what `stream` holds at the
+ * call and the call returns when all of it is done.
  * The copies overlap only when the host buffers are page-locked
  * (cudaHostAlloc / cudaHostRegister); with pageable memory the call is still
  * correct but the copies run one after the other.
@@ -137,8 +140,9 @@ ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, void 
  * Device memory: one stream-ordered block on `stream` for the device copies
  * of all five tensors (plus what attn_fwd itself may take for key splits),
  * freed before the call returns into a memory pool of the library's that keeps
- * it for the next call (a device holds up to the largest block asked for).  The two copy streams are created on a
- * device's first call and reused; calls on the same device serialise on them
+ * it for the next call (a device holds up to the largest block asked for).
+ * The library's streams are created on a device's first call and reused;
+ * calls on the same device serialise on them
  * (the call is synchronous anyway).  Errors: those of attn_fwd, plus
  * ATTN_ERR_NOMEM when the device block cannot be allocated.
  *
