@@ -132,6 +132,7 @@ _COMMON_SOURCES = ("attn_internal.h", "sm100_ptx.cuh", "tma_host.cu", "attn_api.
 KERNEL_SOURCES = {
     "attn_tc2_kernel": ("attn_tc2.cu",) + _COMMON_SOURCES,
     "attn_tc_kernel": ("attn_tc.cu",) + _COMMON_SOURCES,
+    "attn_tcx_kernel": ("attn_tcx.cu",) + _COMMON_SOURCES,
 }
 
 

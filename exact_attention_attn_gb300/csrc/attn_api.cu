@@ -143,6 +143,14 @@ void make_plan(const Problem &p, const DeviceInfo &dev, int splits, attn_plan *p
   }
 }
 
+// The tensor-core kernel for the head dim: two-tile (D 64, 128), cluster
+// Split-D (D 512, 1024), else the Split-D kernel with per-slice scores.
+cudaError_t launch_tensor(const Problem &p, int device, cudaStream_t st) {
+  if (tc2_supports(p.D)) return launch_tc2(p, device, wait_limit_ns(), st);
+  if (tcx_supports(p.D)) return launch_tcx(p, device, wait_limit_ns(), st);
+  return launch_tc(p, device, wait_limit_ns(), st);
+}
+
 int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   switch (plan.path) {
@@ -154,8 +162,7 @@ int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaSt
       break;
     case ATTN_PATH_TC:
       p.kv_splits = 1;
-      e = tc2_supports(p.D) ? launch_tc2(p, dev.device, wait_limit_ns(), st)
-                            : launch_tc(p, dev.device, wait_limit_ns(), st);
+      e = launch_tensor(p, dev.device, st);
       break;
     case ATTN_PATH_TC_SPLITKV: {
       // stream-ordered workspace: allocated and freed on the caller's stream
@@ -168,8 +175,7 @@ int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaSt
       p.kv_splits = plan.kv_splits;
       p.ws_o = static_cast<float *>(ws);
       p.ws_lse = p.ws_o + (int64_t)plan.kv_splits * rows * p.D;
-      e = tc2_supports(p.D) ? launch_tc2(p, dev.device, wait_limit_ns(), st)
-                            : launch_tc(p, dev.device, wait_limit_ns(), st);
+      e = launch_tensor(p, dev.device, st);
       if (e == cudaSuccess) e = launch_combine(p, st);
       cudaError_t f = cudaFreeAsync(ws, st);
       if (e == cudaSuccess) e = f;
