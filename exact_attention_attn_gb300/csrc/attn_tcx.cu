@@ -427,18 +427,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int j = 0; j < nblk && ok; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, abortf, limit))) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_base + TM_S + cc * 32, sr[cc]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
-      tc_fence_before();
-      mbar_arrive(&bars->s_free);  // S may be overwritten by the next block's partial
-      if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(is_owner ? 0 : 3, j);
       const uint32_t pcol = (j & 1) ? TM_P1 : TM_P0;
 
       if (!is_owner) {
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_base + TM_S + cc * 32, sr[cc]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
+        tc_fence_before();
+        mbar_arrive(&bars->s_free);  // S may be overwritten by the next block's partial
+        if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(3, j);
         // -------- sender: partial rows to their owner; the P of the block
         // before is taken afterwards, so that this block's rows are already on
         // their way while the owner works on the previous one
@@ -473,23 +473,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(1, j);
       float x[BN];
       {
-        // sum of the partials in rank order
+        // the other CTAs' partials in rank order, then this CTA's own, read
+        // from TMEM a quarter at a time (its S stays there until now)
         const float4 *slots = reinterpret_cast<const float4 *>(sx + orow * 16);
 #pragma unroll
         for (int c4 = 0; c4 < 32; ++c4) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 acc = slots[c4 * R];
 #pragma unroll
-          for (int q = 0; q < NX; ++q) {
-            float4 v;
-            if (q == (int)me) {
-              v = make_float4(__uint_as_float(sr[c4 >> 3][(c4 & 7) * 4 + 0]),
-                              __uint_as_float(sr[c4 >> 3][(c4 & 7) * 4 + 1]),
-                              __uint_as_float(sr[c4 >> 3][(c4 & 7) * 4 + 2]),
-                              __uint_as_float(sr[c4 >> 3][(c4 & 7) * 4 + 3]));
-            } else {
-              const int sl = q < (int)me ? q : q - 1;
-              v = slots[sl * (XSLOT / 16) + c4 * R];
-            }
+          for (int sl = 1; sl < NX - 1; ++sl) {
+            const float4 v = slots[sl * (XSLOT / 16) + c4 * R];
             acc.x += v.x;
             acc.y += v.y;
             acc.z += v.z;
@@ -500,6 +492,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           x[4 * c4 + 2] = acc.z;
           x[4 * c4 + 3] = acc.w;
         }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + TM_S + cc * 32, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[cc * 32 + i] += __uint_as_float(r[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->s_free);  // S may be overwritten by the next block's partial
+        if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(0, j);
       }
       if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(9, j);
       __syncwarp();
