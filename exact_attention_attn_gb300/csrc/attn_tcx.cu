@@ -89,7 +89,7 @@ struct XParams {
   Problem p;
   int ntiles;
   int kst;
-  uint32_t off_k, off_x, off_p, off_a, off_bar;
+  uint32_t off_k, off_x, off_p, off_a, off_s, off_sa, off_bar;
   uint64_t wait_limit_ns;
 };
 
@@ -104,8 +104,10 @@ struct XBars {
   // stores; one thread of this CTA arrives with the expected byte count
   uint64_t xin_full;  // partial rows of every other CTA have landed here
   uint64_t xin_free;  // every owner has taken this CTA's partial rows
-  uint64_t pin_full[2];  // P rows and rescale factors of every other owner have landed in buffer b
-  uint64_t pin_free[2];  // every other CTA has taken this CTA's P rows from its buffer b
+  uint64_t pin_full;  // P rows and rescale factors of every other owner have landed here
+  uint64_t pin_free;  // every other CTA has taken this CTA's P rows
+  uint64_t stg_full;  // the owner warps have staged this block's P rows (local)
+  uint64_t stg_free;  // the other warps have forwarded the staged rows (local)
   uint64_t fin_full;  // final l and m of every other owner's rows have landed here
   uint64_t done;
   uint32_t tmem_slot;
@@ -170,7 +172,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *sk = smem + prm.off_k;
   uint8_t *sx = smem + prm.off_x;
   uint8_t *sp = smem + prm.off_p;
-  float *salpha = reinterpret_cast<float *>(smem + prm.off_a);  // [2][128]
+  float *salpha = reinterpret_cast<float *>(smem + prm.off_a);  // [128], by tile row
+  uint8_t *sst = smem + prm.off_s;                               // staged own P rows
+  float *sstal = reinterpret_cast<float *>(smem + prm.off_sa);    // staged own rescale factors
   // l[128], m[128] of every row at the end, in the Q region: every CTA's last
   // Q K^T has completed before any owner sends them (it needed their partials)
   float *sfin = reinterpret_cast<float *>(smem);
@@ -217,10 +221,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bars->o_bar[1], 1);
     mbar_init(&bars->xin_full, 1);
     mbar_init(&bars->xin_free, (NX - 1) * OWN_WARPS);
-    for (int b2 = 0; b2 < 2; ++b2) {
-      mbar_init(&bars->pin_full[b2], 1);
-      mbar_init(&bars->pin_free[b2], (NX - 1) * OWN_WARPS);
-    }
+    mbar_init(&bars->pin_full, 1);
+    mbar_init(&bars->pin_free, (NX - 1) * OWN_WARPS);
+    mbar_init(&bars->stg_full, R);
+    mbar_init(&bars->stg_free, 4 - OWN_WARPS);
     mbar_init(&bars->fin_full, 1);
     mbar_init(&bars->done, 1);
     bars->abort = 0;
@@ -371,14 +375,37 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int pslot_in = owner < (int)me ? owner : owner - 1;
     const uint32_t sx_u = smem_u32(sx), sp_u = smem_u32(sp), sa_u = smem_u32(salpha), sf_u = smem_u32(sfin);
 
+    // A sender warp forwards this CTA's staged P rows of block jj (one row per
+    // lane, with its rescale factor) to the CTA that owns the warp's own rows:
+    // at D=1024 each of the three sender warps serves one other CTA, at D=512
+    // the two serve halves of the rows.  The owner warps only stage them.
+    auto forward_p = [&](int jj) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->stg_full, jj & 1, abortf, limit))) return false;
+      if (jj > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->pin_free, (jj - 1) & 1, abortf, limit))) return false;
+      const int fr = (warp % OWN_WARPS) * 32 + lane;  // row among this CTA's owned rows
+      const int ps = (int)me < owner ? (int)me : (int)me - 1;  // this CTA's slot among the target's P senders
+      const uint32_t dst = mapa_shared(sp_u, (uint32_t)owner) + (uint32_t)((ps * R + fr) * 16);
+      const uint32_t rbar = mapa_shared(smem_u32(&bars->pin_full), (uint32_t)owner);
+      const uint4 *src = reinterpret_cast<const uint4 *>(sst + fr * 16);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 w4 = src[c * R];
+        st_async_v4(dst + (uint32_t)(c * NOTHER * 16), w4.x, w4.y, w4.z, w4.w, rbar);
+      }
+      st_async_u32(mapa_shared(sa_u + (uint32_t)((int)me * R + fr) * 4u, (uint32_t)owner), __float_as_uint(sstal[fr]),
+                   rbar);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->stg_free);
+      return true;
+    };
+
     // a sender warp takes P of block jj from its owner: the rescale factor
     // (applied to its O rows once P_{jj-1} V has completed) and the P rows,
     // into TMEM P buffer jj % 2 once P_{jj-2} V has read it
     auto take_p = [&](int jj) -> bool {
-      const int pb = jj & 1;
-      if (lane == 0 && warp == first_sender) mbar_arrive_expect_tx(&bars->pin_full[pb], PBYTES);
-      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->pin_full[pb], (jj >> 1) & 1, abortf, limit))) return false;
-      const float alpha = salpha[pb * BM + row];
+      if (lane == 0 && warp == first_sender) mbar_arrive_expect_tx(&bars->pin_full, PBYTES);
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->pin_full, jj & 1, abortf, limit))) return false;
+      const float alpha = salpha[row];
       if (__any_sync(0xffffffffu, alpha != 1.f) && jj > 0) {
         const int pj = jj - 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_bar[pj & 1], (pj >> 1) & 1, abortf, limit))) return false;
@@ -399,7 +426,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_bar[pj & 1], (pj >> 1) & 1, abortf, limit))) return false;
         tc_fence_after();
       }
-      const uint4 *src = reinterpret_cast<const uint4 *>(sp + pb * (NOTHER * 256) + (pslot_in * R + orow) * 16);
+      const uint4 *src = reinterpret_cast<const uint4 *>(sp + (pslot_in * R + orow) * 16);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
@@ -414,9 +441,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st32(tmem + lane_base + pc + h * 32, pk);
       }
       __syncwarp();
-      if (lane == 0 && jj + 2 < nblk) {  // the owner writes P_{jj+2} into this buffer
-        mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&bars->pin_free[pb]), (uint32_t)owner));
-      }
+      if (lane == 0 && jj + 1 < nblk)  // P_{jj+1} may be written here
+        mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&bars->pin_free), (uint32_t)owner));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[jj & 1]);
@@ -453,11 +479,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           st_async_v4(dst + (uint32_t)(c4 * R * 16), sr[c4 >> 3][(c4 & 7) * 4 + 0], sr[c4 >> 3][(c4 & 7) * 4 + 1],
                       sr[c4 >> 3][(c4 & 7) * 4 + 2], sr[c4 >> 3][(c4 & 7) * 4 + 3], rbar);
         if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(4, j);
-        if (j > 0 && !take_p(j - 1)) {
+        if (j > 0 && !(forward_p(j - 1) && take_p(j - 1))) {
           ok = false;
           break;
         }
-        if (j + 1 == nblk && !take_p(j)) {
+        if (j + 1 == nblk && !(forward_p(j) && take_p(j))) {
           ok = false;
           break;
         }
@@ -565,14 +591,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
       }
-      // P rows go to every other CTA too, into buffer j % 2: P_{j-2} has been taken from it
-      const int pb = j & 1;
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bars->pin_free[pb], ((j - 2) >> 1) & 1, abortf, limit))) {
+      // P rows are staged for the other warps to forward: the previous block's
+      // have been forwarded
+      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->stg_free, (j - 1) & 1, abortf, limit))) {
         ok = false;
         break;
       }
       if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(11, j);
       float lsum = 0.f;
+      uint4 *stg = reinterpret_cast<uint4 *>(sst + orow * 16);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
@@ -584,27 +611,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tmem + lane_base + pcol + h * 32, pk);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) stg[(h * 8 + c) * R] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(12 + h, j);
-#pragma unroll
-        for (int q = 0; q < NX; ++q) {
-          if (q == (int)me) continue;
-          const int ps = (int)me < q ? (int)me : (int)me - 1;  // this CTA's slot among q's P senders
-          const uint32_t dst = mapa_shared(sp_u, (uint32_t)q) + (uint32_t)(pb * (NOTHER * 256) + (ps * R + orow) * 16);
-          const uint32_t rbar = mapa_shared(smem_u32(&bars->pin_full[pb]), (uint32_t)q);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_async_v4(dst + (uint32_t)((h * 8 + c) * NOTHER * 16), pk[4 * c + 0], pk[4 * c + 1], pk[4 * c + 2],
-                        pk[4 * c + 3], rbar);
-        }
       }
       l += lsum;
-      // the rescale factor (its bytes complete the receiver's phase with P's)
-#pragma unroll
-      for (int q = 0; q < NX; ++q) {
-        if (q == (int)me) continue;
-        st_async_u32(mapa_shared(sa_u + (uint32_t)(pb * BM + row) * 4u, (uint32_t)q), __float_as_uint(alpha),
-                     mapa_shared(smem_u32(&bars->pin_full[pb]), (uint32_t)q));
-      }
+      sstal[orow] = alpha;
+      mbar_arrive(&bars->stg_full);
       if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(2, j);
       tmem_wait_st();
       tc_fence_before();
@@ -704,8 +717,10 @@ struct XLayout {
   static constexpr int R = BM / NX;
   static constexpr int QB = 4 * CHUNK_BYTES;
   static constexpr int XB = (NX - 1) * R * 512;
-  static constexpr int PB = 2 * (BM - R) * 256;  // two buffers
-  static constexpr int AB = 2 * BM * 4;
+  static constexpr int PB = (BM - R) * 256;
+  static constexpr int AB = BM * 4;
+  static constexpr int SB = R * 256;
+  static constexpr int SAB = 512;
 };
 
 template <int NX>
@@ -713,7 +728,7 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   using L = XLayout<NX>;
   static_assert(sizeof(XBars) <= 1024, "barrier block too large");
   constexpr int kBarBytes = (int)((sizeof(XBars) + 127) / 128 * 128);
-  const int fixed = L::QB + L::XB + L::PB + L::AB + kBarBytes + 1024 /* alignment */;
+  const int fixed = L::QB + L::XB + L::PB + L::AB + L::SB + L::SAB + kBarBytes + 1024 /* alignment */;
   int kst = (kSmemMax - fixed) / ITEM_BYTES;
   if (kst > MAX_KST) kst = MAX_KST;
   if (kst < 2) return cudaErrorInvalidConfiguration;
@@ -726,7 +741,9 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   prm.off_x = prm.off_k + kst * ITEM_BYTES;
   prm.off_p = prm.off_x + L::XB;
   prm.off_a = prm.off_p + L::PB;
-  prm.off_bar = prm.off_a + L::AB;
+  prm.off_s = prm.off_a + L::AB;
+  prm.off_sa = prm.off_s + L::SB;
+  prm.off_bar = prm.off_sa + L::SAB;
   prm.wait_limit_ns = wait_limit_ns;
   const int smem = (int)prm.off_bar + kBarBytes + 1024;
   if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
