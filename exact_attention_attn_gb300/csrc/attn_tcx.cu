@@ -491,45 +491,41 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
 
       // -------- owner: full scores of its rows, online softmax, P to everyone
+      // this CTA's own partial first, a quarter at a time, so that S may be
+      // overwritten by the next block's while the other CTAs' partials travel
+      float x[BN];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + TM_S + cc * 32, r);
+        tmem_wait_ld();
+        reg_fence32(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[cc * 32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->s_free);
+      if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(0, j);
       if (lane == 0 && warp % OWN_WARPS == 0) mbar_arrive_expect_tx(&bars->xin_full, (NX - 1) * XSLOT);
       if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->xin_full, j & 1, abortf, limit))) {
         ok = false;
         break;
       }
       if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(1, j);
-      float x[BN];
       {
-        // the other CTAs' partials in rank order, then this CTA's own, read
-        // from TMEM a quarter at a time (its S stays there until now)
+        // plus the other CTAs' partials in rank order
         const float4 *slots = reinterpret_cast<const float4 *>(sx + orow * 16);
 #pragma unroll
         for (int c4 = 0; c4 < 32; ++c4) {
-          float4 acc = slots[c4 * R];
 #pragma unroll
-          for (int sl = 1; sl < NX - 1; ++sl) {
+          for (int sl = 0; sl < NX - 1; ++sl) {
             const float4 v = slots[sl * (XSLOT / 16) + c4 * R];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            x[4 * c4 + 0] += v.x;
+            x[4 * c4 + 1] += v.y;
+            x[4 * c4 + 2] += v.z;
+            x[4 * c4 + 3] += v.w;
           }
-          x[4 * c4 + 0] = acc.x;
-          x[4 * c4 + 1] = acc.y;
-          x[4 * c4 + 2] = acc.z;
-          x[4 * c4 + 3] = acc.w;
         }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + TM_S + cc * 32, r);
-          tmem_wait_ld();
-          reg_fence32(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[cc * 32 + i] += __uint_as_float(r[i]);
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->s_free);  // S may be overwritten by the next block's partial
-        if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(0, j);
       }
       if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(9, j);
       __syncwarp();
