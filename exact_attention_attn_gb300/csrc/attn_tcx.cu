@@ -14,8 +14,8 @@
 // rows for them, and runs the online softmax of the "FlashAttention v1/v2/v3/v4"
 // page ("El truco que hizo posible todo: online softmax", with the
 // conditional rescaling of its FA4 section) on the full scores of its rows.
-// It sends P (bf16) and the rescale factors of its rows back to every CTA,
-// and each CTA accumulates O_r += P V_r for its own output slice.  So the
+// P (bf16) and the rescale factors of its rows go back to every CTA, and each
+// CTA accumulates O_r += P V_r for its own output slice.  So the
 // tensor cores do the useful work once (no CTA recomputes S), at the price of
 // moving (NX - 1) R rows of fp32 partial scores and bf16 P per key block
 // through the cluster.
@@ -23,17 +23,20 @@
 // CTA = 8 warps:
 //   warps 0-3  exchange + softmax + epilogue, one tile row per thread (warp w
 //              touches TMEM lanes 32w..32w+31); a warp whose rows this CTA
-//              owns runs the softmax, the others send their partial rows to
-//              the owner and later take P and the rescale factors back
+//              owns runs the softmax and stages its P rows in shared memory;
+//              each other warp sends its partial rows to their owner,
+//              forwards this CTA's staged P rows to that same CTA, and takes
+//              P and the rescale factors of its own rows back
 //   warps 4, 6 TMA producers of the ring (one thread each, alternate items)
 //   warp 5     TMEM allocator and MMA issuer (one thread)
 //   warp 7     idle
 //
-// Shared memory: Q_r resident (64 KB); a ring of 32 KB items in the order
-// K_0, then per block j: K_{j+1} (two items), V_j (two items); xin, the
-// partial rows sent to this CTA (NX - 1 slots of R rows x 128 fp32); pin, the
-// P rows sent to this CTA ((128 - R) rows x 128 bf16); the rescale factors;
-// the final l and m of every row.
+// Shared memory: Q_r resident (64 KB); a ring of 32 KB items (K_0 and K_1,
+// then per block j: K_{j+2}, V_j, two items each); xin, the partial rows sent
+// to this CTA (NX - 1 slots of R rows x 128 fp32); pin, the P rows sent to
+// this CTA ((128 - R) rows x 128 bf16) and their rescale factors; the staged
+// P rows and factors of this CTA's own rows; at the end the final l and m of
+// every row, in the Q region.
 //
 // TMEM columns: S [0,128) fp32 partial scores; P0 [128,192) and P1 [192,256)
 // bf16 pairs (double-buffered); O [256, 512) fp32 output slice.
