@@ -55,6 +55,37 @@ def test_gqa_ratios(Hq, Hkv, causal):
     check_case(2, Hq, Hkv, 300, 300, 128, causal, seed=Hq * 10 + Hkv)
 
 
+# D = 512 and 1024 run on clusters of D/256 CTAs that exchange partial scores
+# and P; these cases cover single-row and single-key problems, key counts
+# below one block, ragged tails, GQA, rows that see no key, and a negative
+# and a zero scale.
+CLUSTER_CASES = [
+    (1, 1, 1, 1, 1, False, None),
+    (1, 2, 2, 129, 3, False, None),
+    (1, 2, 1, 300, 100, True, None),
+    (2, 4, 2, 200, 260, True, None),
+    (1, 1, 1, 64, 700, False, None),
+    (1, 2, 2, 150, 300, False, -0.04),
+    (1, 2, 2, 150, 300, True, 0.0),
+]
+
+
+@pytest.mark.parametrize("D", [512, 1024])
+@pytest.mark.parametrize("case", CLUSTER_CASES, ids=[str(c) for c in CLUSTER_CASES])
+def test_cluster_splitd_cases(D, case):
+    B, Hq, Hkv, Nq, Nkv, causal, scale = case
+    check_case(B, Hq, Hkv, Nq, Nkv, D, causal, seed=Nq + Nkv + D, scale=scale)
+
+
+@pytest.mark.parametrize("D", [512, 1024])
+def test_cluster_splitd_deterministic(D):
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 2, 300, 500, D, 23))
+    o1, l1 = attn_fwd(q, k, v, causal=True)
+    o2, l2 = attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 @pytest.mark.parametrize("D", [128, 512])
 def test_large_scores(D):
     # scale 1 on amp-2 inputs: scores of order 2*sqrt(D)*2; stresses the running max
