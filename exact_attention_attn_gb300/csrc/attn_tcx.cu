@@ -105,7 +105,7 @@ struct XBars {
   uint64_t o_bar[2];
   // the *_full barriers count the bytes of the other CTAs' asynchronous
   // stores; one thread of this CTA arrives with the expected byte count
-  uint64_t xin_full;  // partial rows of every other CTA have landed here
+  uint64_t xin_full[3];  // partial rows of the other CTA in slot s have landed here
   uint64_t xin_free;  // every owner has taken this CTA's partial rows
   uint64_t pin_full;  // P rows and rescale factors of every other owner have landed here
   uint64_t pin_free;  // every other CTA has taken this CTA's P rows
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bars->p_full[1], 128);
     mbar_init(&bars->o_bar[0], 1);
     mbar_init(&bars->o_bar[1], 1);
-    mbar_init(&bars->xin_full, 1);
+    for (int sl = 0; sl < NX - 1; ++sl) mbar_init(&bars->xin_full[sl], 1);
     mbar_init(&bars->xin_free, (NX - 1) * OWN_WARPS);
     mbar_init(&bars->pin_full, 1);
     mbar_init(&bars->pin_free, (NX - 1) * OWN_WARPS);
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         const uint32_t dst = mapa_shared(sx_u, (uint32_t)owner) + (uint32_t)(xslot_out * XSLOT + orow * 16);
-        const uint32_t rbar = mapa_shared(smem_u32(&bars->xin_full), (uint32_t)owner);
+        const uint32_t rbar = mapa_shared(smem_u32(&bars->xin_full[xslot_out]), (uint32_t)owner);
 #pragma unroll
         for (int c4 = 0; c4 < 32; ++c4)
           st_async_v4(dst + (uint32_t)(c4 * R * 16), sr[c4 >> 3][(c4 & 7) * 4 + 0], sr[c4 >> 3][(c4 & 7) * 4 + 1],
@@ -509,19 +509,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(&bars->s_free);
       if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(0, j);
-      if (lane == 0 && warp % OWN_WARPS == 0) mbar_arrive_expect_tx(&bars->xin_full, (NX - 1) * XSLOT);
-      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->xin_full, j & 1, abortf, limit))) {
-        ok = false;
-        break;
-      }
-      if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(1, j);
+      if (lane == 0 && warp % OWN_WARPS == 0)
+        for (int sl = 0; sl < NX - 1; ++sl) mbar_arrive_expect_tx(&bars->xin_full[sl], XSLOT);
       {
-        // plus the other CTAs' partials in rank order
+        // plus the other CTAs' partials in rank order, each as soon as it has
+        // landed (the order of the additions stays fixed)
         const float4 *slots = reinterpret_cast<const float4 *>(sx + orow * 16);
 #pragma unroll
-        for (int c4 = 0; c4 < 32; ++c4) {
+        for (int sl = 0; sl < NX - 1; ++sl) {
+          if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bars->xin_full[sl], j & 1, abortf, limit))) {
+            ok = false;
+            break;
+          }
+          if (sl == 0 && lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(1, j);
 #pragma unroll
-          for (int sl = 0; sl < NX - 1; ++sl) {
+          for (int c4 = 0; c4 < 32; ++c4) {
             const float4 v = slots[sl * (XSLOT / 16) + c4 * R];
             x[4 * c4 + 0] += v.x;
             x[4 * c4 + 1] += v.y;
@@ -530,6 +532,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
+      if (!ok) break;
       if (lane == 0 && (warp & (OWN_WARPS - 1)) == 0) TCX_EV(9, j);
       __syncwarp();
       if (lane == 0 && j + 1 < nblk) {
