@@ -147,7 +147,10 @@ void make_plan(const Problem &p, const DeviceInfo &dev, int splits, attn_plan *p
 // Split-D (D 512, 1024), else the Split-D kernel with per-slice scores.
 cudaError_t launch_tensor(const Problem &p, int device, cudaStream_t st) {
   if (tc2_supports(p.D)) return launch_tc2(p, device, wait_limit_ns(), st);
-  if (tcx_supports(p.D)) return launch_tcx(p, device, wait_limit_ns(), st);
+  if (tcx_supports(p.D) && !(debug_flags() & ATTN_DEBUG_NO_CLUSTER)) {
+    const cudaError_t e = launch_tcx(p, device, wait_limit_ns(), st);
+    if (e != cudaErrorNotSupported) return e;  // else no room for the cluster: per-slice kernel
+  }
   return launch_tc(p, device, wait_limit_ns(), st);
 }
 
@@ -235,7 +238,7 @@ const char *attn_strerror(int code) {
 const char *attn_last_cuda_error(void) { return attn::t_last_error; }
 
 int attn_set_debug(int flags, long long wait_limit_ns) {
-  if (flags & ~ATTN_DEBUG_DROP_V_COPY) return ATTN_ERR_ARG;
+  if (flags & ~(ATTN_DEBUG_DROP_V_COPY | ATTN_DEBUG_NO_CLUSTER)) return ATTN_ERR_ARG;
   if (wait_limit_ns < 0) return ATTN_ERR_ARG;
   attn::g_debug_flags.store(flags);
   attn::g_wait_limit_ns.store(wait_limit_ns == 0 ? (long long)attn::kWaitLimitNs : wait_limit_ns);

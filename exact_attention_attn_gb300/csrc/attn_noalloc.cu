@@ -92,9 +92,14 @@ extern "C" int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void
   p.ws_o = scratch;
   p.ws_lse = scratch + (int64_t)kv_splits * rows * D;  // 16-byte aligned: D is a multiple of 64
   const uint64_t limit = 2000000000ull;  // the same 2 s bound on device-side waits as attn_fwd
-  e = tc2_supports(D)   ? launch_tc2(p, device, limit, st)
-      : tcx_supports(D) ? launch_tcx(p, device, limit, st)
-                        : launch_tc(p, device, limit, st);
+  if (tc2_supports(D)) {
+    e = launch_tc2(p, device, limit, st);
+  } else {
+    // the cluster kernel where it fits on the device, else the per-slice one
+    e = tcx_supports(D) && !(debug_flags() & ATTN_DEBUG_NO_CLUSTER) ? launch_tcx(p, device, limit, st)
+                                                                  : cudaErrorNotSupported;
+    if (e == cudaErrorNotSupported) e = launch_tc(p, device, limit, st);
+  }
   if (e == cudaSuccess) e = launch_combine(p, st);
   return e == cudaSuccess ? ATTN_OK : record_cuda_error(e);
 }

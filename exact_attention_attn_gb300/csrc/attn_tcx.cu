@@ -775,6 +775,21 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // a device that cannot hold one such cluster at a time (a partitioned GPU,
+  // say) gets cudaErrorNotSupported, and the caller the per-slice kernel
+  static std::atomic<int> fits[64];  // 0 unknown, 1 yes, 2 no
+  int f = fits[device].load(std::memory_order_relaxed);
+  if (f == 0) {
+    int nclusters = 0;
+    cudaError_t q = cudaOccupancyMaxActiveClusters(&nclusters, attn_tcx_kernel<NX>, &cfg);
+    if (q != cudaSuccess) {
+      cudaGetLastError();
+      nclusters = 0;
+    }
+    f = nclusters > 0 ? 1 : 2;
+    fits[device].store(f, std::memory_order_relaxed);
+  }
+  if (f != 1) return cudaErrorNotSupported;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tcx_kernel<NX>, tq, tk, tv, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

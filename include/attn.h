@@ -203,17 +203,23 @@ ATTN_API int attn_fwd_status(attn_stream_t stream);
  * attn_set_debug -- test support for the failure path; process-wide, read at
  * every later launch.
  *
- * flags: 0 or ATTN_DEBUG_DROP_V_COPY, which makes the V producer of the
- *   head-dim-64/128 kernel skip its copy of each CTA's second key block, so
- *   the MMA thread's wait for it runs out: the kernel then records
- *   ATTN_ERR_TIMEOUT in the status word, every role of the CTA stops waiting,
- *   drains its own copies and MMAs, frees its tensor memory and exits (no
- *   trap, no hang; outputs of that call are undefined).
+ * flags: an OR of
+ *   ATTN_DEBUG_DROP_V_COPY, which makes the V producer of the head-dim-64/128
+ *     kernel skip its copy of each CTA's second key block, so the MMA
+ *     thread's wait for it runs out: the kernel then records ATTN_ERR_TIMEOUT
+ *     in the status word, every role of the CTA stops waiting, drains its own
+ *     copies and MMAs, frees its tensor memory and exits (no trap, no hang;
+ *     outputs of that call are undefined);
+ *   ATTN_DEBUG_NO_CLUSTER, which runs head dims 512 and 1024 on the
+ *     per-slice Split-D kernel (each output slice recomputes the scores)
+ *     instead of the cluster kernel, the path a device takes when it cannot
+ *     hold one cluster; results agree within the parity tolerances.
  * wait_limit_ns: bound on every device-side wait; 0 restores the default
  *   (2 s).
  * Returns ATTN_OK or ATTN_ERR_ARG.
  */
 #define ATTN_DEBUG_DROP_V_COPY 1
+#define ATTN_DEBUG_NO_CLUSTER 2
 ATTN_API int attn_set_debug(int flags, long long wait_limit_ns);
 
 /* Static description of a return code. */

@@ -78,6 +78,18 @@ def test_cluster_splitd_cases(D, case):
 
 
 @pytest.mark.parametrize("D", [512, 1024])
+@pytest.mark.parametrize("causal", [False, True])
+def test_per_slice_path(D, causal):
+    # the path taken where a cluster does not fit: each output slice recomputes S
+    from exact_attention_attn_gb300 import attn_set_debug
+    attn_set_debug(2)  # ATTN_DEBUG_NO_CLUSTER
+    try:
+        check_case(1, 2, 1, 200, 330, D, causal, seed=D + 3 * causal)
+    finally:
+        attn_set_debug(0)
+
+
+@pytest.mark.parametrize("D", [512, 1024])
 def test_cluster_splitd_deterministic(D):
     q, k, v = (t.cuda() for t in make_qkv(1, 2, 2, 300, 500, D, 23))
     o1, l1 = attn_fwd(q, k, v, causal=True)
