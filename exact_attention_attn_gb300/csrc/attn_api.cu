@@ -85,10 +85,17 @@ int check_sizes(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal) {
 constexpr int kMaxSplits = 64;
 
 // CTAs of the tensor-core launch for one key range per query tile.
+// D-slices per 128-row tile: the cluster kernel's CTAs per cluster where it
+// runs, else the per-slice kernel's output slices.
+int d_slices(int D) {
+  const int nx = (debug_flags() & ATTN_DEBUG_NO_CLUSTER) ? 0 : tcx_slices(D);
+  return nx > 0 ? nx : tc_config(D).nslices;
+}
+
 int64_t base_ctas(const Problem &p) {
   const int64_t tiles = (p.Nq + 127) / 128;
   if (tc2_supports(p.D)) return ((tiles + 1) / 2) * p.B * p.Hq;
-  return tiles * p.B * p.Hq * tc_config(p.D).nslices;
+  return tiles * p.B * p.Hq * d_slices(p.D);
 }
 
 // Key-range splits when one CTA per query tile leaves SMs idle: the split
@@ -131,7 +138,7 @@ void make_plan(const Problem &p, const DeviceInfo &dev, int splits, attn_plan *p
   }
   const int s = splits > 0 ? splits : auto_splits(p, dev.sm_count);
   plan->kv_splits = s;
-  plan->d_slices = tc2_supports(p.D) ? 1 : tc_config(p.D).nslices;
+  plan->d_slices = tc2_supports(p.D) ? 1 : d_slices(p.D);
   plan->grid = (int)(base_ctas(p) * s);
   if (s == 1) {
     plan->path = ATTN_PATH_TC;

@@ -68,11 +68,12 @@ TcConfig tc_config(int D);
 // Nkv >= 1.  Bounded waits give up after wait_limit_ns.
 cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream);
 
-// Cluster Split-D kernel for head dims 512 and 1024: the D / 256 output
-// slices of a tile are the CTAs of one cluster, which compute the scores
-// once (partial products over their slices, summed through distributed
-// shared memory).
+// Cluster Split-D kernel for head dims 384, 512, 768 and 1024: the output
+// slices of a tile (2 or 4) are the CTAs of one cluster, which compute the
+// scores once (partial products over their slices, summed through
+// distributed shared memory).
 bool tcx_supports(int D);
+int tcx_slices(int D);  // CTAs per cluster (D-slices per tile), 0 when not supported
 cudaError_t launch_tcx(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream);
 
 // Two-tile ping-pong tensor-core kernel for head dims 64 and 128.

@@ -1,13 +1,14 @@
-// Exact attention forward for head dims 512 and 1024: Split-D across a
-// thread-block cluster, the scores computed once.
+// Exact attention forward for head dims 384, 512, 768 and 1024: Split-D
+// across a thread-block cluster, the scores computed once.
 //
 // The FFPA page's Split-D cuts the D axis into chunks so that on-chip memory
 // does not grow with D.  On sm_103a the output accumulator of a 128-row tile
 // lives in TMEM, which holds at most 256 fp32 output columns next to S and P,
-// so a tile's output is cut into NX = D / 256 slices.  Here the NX slices of a
-// tile are the NX CTAs of one cluster, and the contraction of S = Q K^T is cut
-// the same way: CTA r keeps Q[:, 256r, 256r + 256) in shared memory, streams
-// the matching columns of K and V, and computes the partial scores
+// so a tile's output is cut into NX slices of W = D / NX <= 256 columns (NX =
+// 2 for D = 384, 512; 4 for D = 768, 1024).  Here the NX slices of a tile are
+// the NX CTAs of one cluster, and the contraction of S = Q K^T is cut the
+// same way: CTA r keeps Q[:, Wr, Wr + W) in shared memory, streams the
+// matching columns of K and V, and computes the partial scores
 // S_r = Q_r K_r^T on its tensor cores.  The partials are summed across the
 // cluster through distributed shared memory: CTA r owns rows
 // [rR, rR + R) (R = 128 / NX) of the tile, receives the other CTAs' partial
@@ -31,8 +32,9 @@
 //   warp 5     TMEM allocator and MMA issuer (one thread)
 //   warp 7     idle
 //
-// Shared memory: Q_r resident (64 KB); a ring of 32 KB items (K_0 and K_1,
-// then per block j: K_{j+2}, V_j, two items each); xin, the partial rows sent
+// Shared memory: Q_r resident (W x 128 bf16); a ring of items of two 64-column
+// chunks (W = 256) or three (W = 192) (K_0 and K_1, then per block j: K_{j+2},
+// V_j); xin, the partial rows sent
 // to this CTA (NX - 1 slots of R rows x 128 fp32); pin, the P rows sent to
 // this CTA ((128 - R) rows x 128 bf16) and their rescale factors; the staged
 // P rows and factors of this CTA's own rows; at the end the final l and m of
@@ -77,7 +79,6 @@ using namespace ptx;
 
 constexpr int BM = 128, BN = 128;
 constexpr int CHUNK_BYTES = 128 * 128;   // one 128-row x 64-column bf16 chunk
-constexpr int ITEM_BYTES = 2 * CHUNK_BYTES;
 constexpr int THREADS = 256;
 constexpr int WARP_LOAD0 = 4, WARP_MMA = 5, WARP_LOAD1 = 6;
 constexpr uint32_t TMEM_COLS = 512;
@@ -118,34 +119,35 @@ struct XBars {
   int slot_item[MAX_KST];
 };
 
-// Ring item i, in the order the MMA thread consumes them: K_0 and K_1 (two
-// items each), then for each block g the two items of K_{g+2} (while there is
-// one) and the two of V_g -- S runs two blocks ahead of P V.
+// Ring item i, in the order the MMA thread consumes them: K_0 and K_1 (NI
+// items each), then for each block g the items of K_{g+2} (while there is
+// one) and those of V_g -- S runs two blocks ahead of P V.
 struct XItem {
   bool is_v;
   int blk, idx;
 };
+template <int NI>  // items per K or V block
 __device__ __forceinline__ XItem ring_item(int i, int nblk) {
   XItem r;
-  const int head = nblk > 1 ? 4 : 2;
+  const int head = (nblk > 1 ? 2 : 1) * NI;
   if (i < head) {
     r.is_v = false;
-    r.blk = i >> 1;
-    r.idx = i & 1;
+    r.blk = i / NI;
+    r.idx = i % NI;
     return r;
   }
   i -= head;
   const int g4 = nblk > 2 ? nblk - 2 : 0;  // groups with a K block
-  if (i < 4 * g4) {
-    const int g = i >> 2, m = i & 3;
-    r.is_v = m >= 2;
+  if (i < 2 * NI * g4) {
+    const int g = i / (2 * NI), m = i % (2 * NI);
+    r.is_v = m >= NI;
     r.blk = r.is_v ? g : g + 2;
-    r.idx = m & 1;
+    r.idx = m % NI;
   } else {
-    i -= 4 * g4;
+    i -= 2 * NI * g4;
     r.is_v = true;
-    r.blk = g4 + (i >> 1);
-    r.idx = i & 1;
+    r.blk = g4 + i / NI;
+    r.idx = i % NI;
   }
   return r;
 }
@@ -160,10 +162,16 @@ __device__ __forceinline__ void raise_abort_cluster(XBars *bars, int *status, ui
     if ((uint32_t)q != me) st_cluster_u32(mapa_shared(a, (uint32_t)q), 1u);
 }
 
-template <int NX>
+// NX CTAs per cluster, each with a slice of SC 64-column chunks (D = 64 NX SC);
+// K and V travel through the ring as NI items of IC chunks per block.
+template <int NX, int SC>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tcx_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ XParams prm) {
+  constexpr int IC = SC % 2 == 0 ? 2 : SC;  // chunks per ring item
+  constexpr int NI = SC / IC;               // ring items per K or V block
+  constexpr int ITEM_BYTES = IC * CHUNK_BYTES;
+  constexpr int OCOLS = SC * 64;            // output columns of the slice
   constexpr int R = BM / NX;           // rows owned by each CTA
   constexpr int OWN_WARPS = R / 32;    // warps holding them
   constexpr int NOTHER = BM - R;       // rows owned by the other CTAs
@@ -202,7 +210,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
   const int q0 = tile * BM;
-  const int c0 = 4 * (int)me;  // first 64-column chunk of this CTA's slice
+  const int c0 = SC * (int)me;  // first 64-column chunk of this CTA's slice
   const int shift = p.Nkv - p.Nq;
   int kv_end = p.Nkv;
   if (p.causal) kv_end = max(0, min(p.Nkv, q0 + BM - 1 + shift + 1));
@@ -253,18 +261,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(&bars->q_full, 4 * CHUNK_BYTES);
+        mbar_arrive_expect_tx(&bars->q_full, SC * CHUNK_BYTES);
         tma_load_4d(sq, &tm_q, &bars->q_full, 0, q0, c0, bh);
       }
-      const int total = 4 * nblk;
+      const int total = 2 * NI * nblk;
       for (int i = r; i < total; i += 2) {
         const int s = i % prm.kst;
         if (!mbar_wait(&bars->k_empty[s], ((i / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars->k_full[s], ITEM_BYTES);
         *reinterpret_cast<volatile int *>(&bars->slot_item[s]) = i;
-        const XItem it = ring_item(i, nblk);
+        const XItem it = ring_item<NI>(i, nblk);
         tma_load_4d(sk + s * ITEM_BYTES, it.is_v ? &tm_v : &tm_k, &bars->k_full[s], 0, (jb + it.blk) * BN,
-                    c0 + 2 * it.idx, bkv);
+                    c0 + IC * it.idx, bkv);
       }
       if (!ok) raise_abort_cluster<NX>(bars, p.status, me);
       // drain: copies of this thread that are still the latest in their slot
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nblk > 0) {
       const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
-      const uint32_t idesc_v = idesc_bf16(BM, 128, 0, 1);
+      const uint32_t idesc_v = idesc_bf16(BM, IC * 64, 0, 1);
       constexpr uint64_t kChunkD = CHUNK_BYTES >> 4, kItemD = ITEM_BYTES >> 4;
       const uint64_t qd = smem_desc(smem_u32(sq), 16, 1024);
       const uint64_t kd_ring = smem_desc(smem_u32(sk), 16, 1024);
@@ -300,16 +308,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       (void)nissued;
       // S_r = Q_r K_r^T over this CTA's 256 columns: two items of two chunks
       auto issue_s = [&]() -> bool {
-        for (int it = 0; it < 2; ++it) {
+        for (int it = 0; it < NI; ++it) {
           int ks;
           if (!next_item(ks)) return false;
           tc_fence_after();
           const uint64_t kd = kd_ring + (uint64_t)ks * kItemD;
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
+          for (int cc = 0; cc < IC; ++cc)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tmem + TM_S, qd + (uint64_t)((2 * it + cc) * kChunkD + kk * 2),
+              mma_ss(tmem + TM_S, qd + (uint64_t)((IC * it + cc) * kChunkD + kk * 2),
                      kd + (uint64_t)(cc * kChunkD + kk * 2), idesc_s, (it | cc | kk) != 0);
           mma_commit(&bars->k_empty[ks]);
         }
@@ -337,15 +345,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abortf, limit)) { ok = false; break; }
         TCX_EV(8, j);
         const uint32_t pcol = tmem + ((j & 1) ? TM_P1 : TM_P0);
-        // O_r += P V_r: two items of 128 output columns
-        for (int v = 0; v < 2 && ok; ++v) {
+        // O_r += P V_r: NI items of IC * 64 output columns
+        for (int v = 0; v < NI && ok; ++v) {
           int vs;
           if (!next_item(vs)) { ok = false; break; }
           tc_fence_after();
           const uint64_t vd = vd_ring + (uint64_t)vs * kItemD;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + TM_O + 128 * v, pcol + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), idesc_v,
+            mma_ts(tmem + TM_O + IC * 64 * v, pcol + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), idesc_v,
                    (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars->k_empty[vs]);
         }
@@ -413,7 +421,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int pj = jj - 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_bar[pj & 1], (pj >> 1) & 1, abortf, limit))) return false;
         tc_fence_after();
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int cc = 0; cc < OCOLS / 32; ++cc) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + TM_O + cc * 32, r);
           tmem_wait_ld();
@@ -571,7 +579,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          for (int cc = 0; cc < 8; ++cc) {
+          for (int cc = 0; cc < OCOLS / 32; ++cc) {
             uint32_t r[32];
             tmem_ld32(tmem + lane_base + TM_O + cc * 32, r);
             tmem_wait_ld();
@@ -663,7 +671,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t row_idx = (int64_t)bh * p.Nq + qi;
       __nv_bfloat16 *obase = p.o + row_idx * p.D + c0 * 64;
       float *wbase = (nsplit > 1) ? p.ws_o + ((int64_t)split * BH * p.Nq + row_idx) * p.D + c0 * 64 : nullptr;
-      for (int cc = 0; cc < 8; ++cc) {
+      for (int cc = 0; cc < OCOLS / 32; ++cc) {
         uint32_t r[32];
         if (nblk > 0) {
           tmem_ld32(tmem + lane_base + TM_O + cc * 32, r);
@@ -714,10 +722,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int NX>
+template <int NX, int SC>
 struct XLayout {
   static constexpr int R = BM / NX;
-  static constexpr int QB = 4 * CHUNK_BYTES;
+  static constexpr int QB = SC * CHUNK_BYTES;
+  static constexpr int IC = SC % 2 == 0 ? 2 : SC;
+  static constexpr int ITEM_BYTES = IC * CHUNK_BYTES;
   static constexpr int XB = (NX - 1) * R * 512;
   static constexpr int PB = (BM - R) * 256;
   static constexpr int AB = BM * 4;
@@ -725,9 +735,10 @@ struct XLayout {
   static constexpr int SAB = 512;
 };
 
-template <int NX>
+template <int NX, int SC>
 cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
-  using L = XLayout<NX>;
+  using L = XLayout<NX, SC>;
+  constexpr int ITEM_BYTES = L::ITEM_BYTES;
   static_assert(sizeof(XBars) <= 1024, "barrier block too large");
   constexpr int kBarBytes = (int)((sizeof(XBars) + 127) / 128 * 128);
   const int fixed = L::QB + L::XB + L::PB + L::AB + L::SB + L::SAB + kBarBytes + 1024 /* alignment */;
@@ -750,13 +761,13 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   const int smem = (int)prm.off_bar + kBarBytes + 1024;
   if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
-  if (!make_chunk_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq, BM, 4)) return cudaErrorInvalidValue;
-  if (!make_chunk_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv, BN, 2)) return cudaErrorInvalidValue;
-  if (!make_chunk_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv, BN, 2)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq, BM, SC)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv, BN, L::IC)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv, BN, L::IC)) return cudaErrorInvalidValue;
   static std::atomic<int> attr_set[64];
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[device].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tcx_kernel<NX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    cudaError_t e = cudaFuncSetAttribute(attn_tcx_kernel<NX, SC>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
     attr_set[device].store(1, std::memory_order_release);
   }
@@ -781,7 +792,7 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   int f = fits[device].load(std::memory_order_relaxed);
   if (f == 0) {
     int nclusters = 0;
-    cudaError_t q = cudaOccupancyMaxActiveClusters(&nclusters, attn_tcx_kernel<NX>, &cfg);
+    cudaError_t q = cudaOccupancyMaxActiveClusters(&nclusters, attn_tcx_kernel<NX, SC>, &cfg);
     if (q != cudaSuccess) {
       cudaGetLastError();
       nclusters = 0;
@@ -790,25 +801,32 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
     fits[device].store(f, std::memory_order_relaxed);
   }
   if (f != 1) return cudaErrorNotSupported;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tcx_kernel<NX>, tq, tk, tv, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tcx_kernel<NX, SC>, tq, tk, tv, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
 
+int tcx_slices(int D) {
+  if (!tcx_supports(D)) return 0;
+  return D == 384 || D == 512 ? 2 : 4;
+}
+
 bool tcx_supports(int D) {
 #ifdef ATTN_NO_TCX
   (void)D;
   return false;
 #else
-  return D == 512 || D == 1024;
+  return D == 384 || D == 512 || D == 768 || D == 1024;
 #endif
 }
 
 cudaError_t launch_tcx(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
-  if (p.D == 512) return launch_tcx_n<2>(p, device, wait_limit_ns, stream);
-  if (p.D == 1024) return launch_tcx_n<4>(p, device, wait_limit_ns, stream);
+  if (p.D == 384) return launch_tcx_n<2, 3>(p, device, wait_limit_ns, stream);
+  if (p.D == 512) return launch_tcx_n<2, 4>(p, device, wait_limit_ns, stream);
+  if (p.D == 768) return launch_tcx_n<4, 3>(p, device, wait_limit_ns, stream);
+  if (p.D == 1024) return launch_tcx_n<4, 4>(p, device, wait_limit_ns, stream);
   return cudaErrorInvalidValue;
 }
 
