@@ -68,7 +68,7 @@ TcConfig tc_config(int D);
 // Nkv >= 1.  Bounded waits give up after wait_limit_ns.
 cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream);
 
-// Cluster Split-D kernel for head dims 384, 512, 768 and 1024: the output
+// Cluster Split-D kernel for head dims 384 ... 1024: the output
 // slices of a tile (2 or 4) are the CTAs of one cluster, which compute the
 // scores once (partial products over their slices, summed through
 // distributed shared memory).

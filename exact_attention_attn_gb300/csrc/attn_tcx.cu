@@ -1,11 +1,12 @@
-// Exact attention forward for head dims 384, 512, 768 and 1024: Split-D
-// across a thread-block cluster, the scores computed once.
+// Exact attention forward for head dims 384 ... 1024 (multiples of 64):
+// Split-D across a thread-block cluster, the scores computed once.
 //
 // The FFPA page's Split-D cuts the D axis into chunks so that on-chip memory
 // does not grow with D.  On sm_103a the output accumulator of a 128-row tile
 // lives in TMEM, which holds at most 256 fp32 output columns next to S and P,
-// so a tile's output is cut into NX slices of W = D / NX <= 256 columns (NX =
-// 2 for D = 384, 512; 4 for D = 768, 1024).  Here the NX slices of a tile are
+// so a tile's output is cut into NX slices of at most 256 columns (NX = 2 up
+// to D = 512, 4 above; slices of equal width where D/64 divides by NX, else
+// widths differing by one 64-column chunk).  Here the NX slices of a tile are
 // the NX CTAs of one cluster, and the contraction of S = Q K^T is cut the
 // same way: CTA r keeps Q[:, Wr, Wr + W) in shared memory, streams the
 // matching columns of K and V, and computes the partial scores
@@ -32,13 +33,13 @@
 //   warp 5     TMEM allocator and MMA issuer (one thread)
 //   warp 7     idle
 //
-// Shared memory: Q_r resident (W x 128 bf16); a ring of items of two 64-column
-// chunks (W = 256) or three (W = 192) (K_0 and K_1, then per block j: K_{j+2},
-// V_j); xin, the partial rows sent
-// to this CTA (NX - 1 slots of R rows x 128 fp32); pin, the P rows sent to
-// this CTA ((128 - R) rows x 128 bf16) and their rescale factors; the staged
-// P rows and factors of this CTA's own rows; at the end the final l and m of
-// every row, in the Q region.
+// Shared memory: Q_r resident (W x 128 bf16 for a slice of W columns); a ring
+// of items of two 64-column chunks (W = 256), three (W = 192) or one (uneven
+// slices), in the order K_0, K_1, then per block j: K_{j+2}, V_j; xin, the
+// partial rows sent to this CTA (NX - 1 slots of R rows x 128 fp32); pin, the
+// P rows sent to this CTA ((128 - R) rows x 128 bf16) and their rescale
+// factors; the staged P rows and factors of this CTA's own rows; at the end
+// the final l and m of every row, in the Q region.
 //
 // TMEM columns: S [0,128) fp32 partial scores; P0 [128,192) and P1 [192,256)
 // bf16 pairs (double-buffered); O [256, 512) fp32 output slice.
@@ -86,7 +87,7 @@ constexpr uint32_t TM_S = 0, TM_P0 = 128, TM_P1 = 192, TM_O = 256;
 constexpr float TAU = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int MAX_KST = 4;
+constexpr int MAX_KST = 8;
 constexpr int kSmemMax = 232448;
 
 struct XParams {
@@ -126,8 +127,7 @@ struct XItem {
   bool is_v;
   int blk, idx;
 };
-template <int NI>  // items per K or V block
-__device__ __forceinline__ XItem ring_item(int i, int nblk) {
+__device__ __forceinline__ XItem ring_item(int i, int nblk, int NI /* items per K or V block */) {
   XItem r;
   const int head = (nblk > 1 ? 2 : 1) * NI;
   if (i < head) {
@@ -162,16 +162,16 @@ __device__ __forceinline__ void raise_abort_cluster(XBars *bars, int *status, ui
     if ((uint32_t)q != me) st_cluster_u32(mapa_shared(a, (uint32_t)q), 1u);
 }
 
-// NX CTAs per cluster, each with a slice of SC 64-column chunks (D = 64 NX SC);
-// K and V travel through the ring as NI items of IC chunks per block.
-template <int NX, int SC>
+// NX CTAs per cluster, each with a slice of SC 64-column chunks (D = 64 NX SC),
+// K and V travelling through the ring as items of IC chunks -- or, UN, slices
+// of SC or SC - 1 chunks (D = 64 nc with nc not a multiple of NX) whose K and
+// V travel as one-chunk items.
+template <int NX, int SC, bool UN>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tcx_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ XParams prm) {
-  constexpr int IC = SC % 2 == 0 ? 2 : SC;  // chunks per ring item
-  constexpr int NI = SC / IC;               // ring items per K or V block
+  constexpr int IC = UN ? 1 : SC % 2 == 0 ? 2 : SC;  // chunks per ring item
   constexpr int ITEM_BYTES = IC * CHUNK_BYTES;
-  constexpr int OCOLS = SC * 64;            // output columns of the slice
   constexpr int R = BM / NX;           // rows owned by each CTA
   constexpr int OWN_WARPS = R / 32;    // warps holding them
   constexpr int NOTHER = BM - R;       // rows owned by the other CTAs
@@ -210,7 +210,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
   const int q0 = tile * BM;
-  const int c0 = SC * (int)me;  // first 64-column chunk of this CTA's slice
+  const int nc = p.D / 64;
+  const int sc = UN ? nc / NX + ((int)me < nc % NX ? 1 : 0) : SC;  // chunks of this CTA's slice
+  const int c0 = UN ? (int)me * (nc / NX) + min((int)me, nc % NX) : SC * (int)me;  // its first chunk
+  const int NI = sc / IC;      // ring items per K or V block
+  const int OCOLS = sc * 64;   // output columns of the slice
   const int shift = p.Nkv - p.Nq;
   int kv_end = p.Nkv;
   if (p.causal) kv_end = max(0, min(p.Nkv, q0 + BM - 1 + shift + 1));
@@ -261,8 +265,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(&bars->q_full, SC * CHUNK_BYTES);
-        tma_load_4d(sq, &tm_q, &bars->q_full, 0, q0, c0, bh);
+        mbar_arrive_expect_tx(&bars->q_full, sc * CHUNK_BYTES);
+        if constexpr (UN) {
+          for (int c = 0; c < sc; ++c) tma_load_4d(sq + c * CHUNK_BYTES, &tm_q, &bars->q_full, 0, q0, c0 + c, bh);
+        } else {
+          tma_load_4d(sq, &tm_q, &bars->q_full, 0, q0, c0, bh);
+        }
       }
       const int total = 2 * NI * nblk;
       for (int i = r; i < total; i += 2) {
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&bars->k_empty[s], ((i / prm.kst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars->k_full[s], ITEM_BYTES);
         *reinterpret_cast<volatile int *>(&bars->slot_item[s]) = i;
-        const XItem it = ring_item<NI>(i, nblk);
+        const XItem it = ring_item(i, nblk, NI);
         tma_load_4d(sk + s * ITEM_BYTES, it.is_v ? &tm_v : &tm_k, &bars->k_full[s], 0, (jb + it.blk) * BN,
                     c0 + IC * it.idx, bkv);
       }
@@ -722,11 +730,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int NX, int SC>
+template <int NX, int SC, bool UN>
 struct XLayout {
   static constexpr int R = BM / NX;
   static constexpr int QB = SC * CHUNK_BYTES;
-  static constexpr int IC = SC % 2 == 0 ? 2 : SC;
+  static constexpr int IC = UN ? 1 : SC % 2 == 0 ? 2 : SC;
   static constexpr int ITEM_BYTES = IC * CHUNK_BYTES;
   static constexpr int XB = (NX - 1) * R * 512;
   static constexpr int PB = (BM - R) * 256;
@@ -735,9 +743,9 @@ struct XLayout {
   static constexpr int SAB = 512;
 };
 
-template <int NX, int SC>
+template <int NX, int SC, bool UN>
 cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
-  using L = XLayout<NX, SC>;
+  using L = XLayout<NX, SC, UN>;
   constexpr int ITEM_BYTES = L::ITEM_BYTES;
   static_assert(sizeof(XBars) <= 1024, "barrier block too large");
   constexpr int kBarBytes = (int)((sizeof(XBars) + 127) / 128 * 128);
@@ -761,13 +769,13 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   const int smem = (int)prm.off_bar + kBarBytes + 1024;
   if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
-  if (!make_chunk_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq, BM, SC)) return cudaErrorInvalidValue;
+  if (!make_chunk_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq, BM, UN ? 1 : SC)) return cudaErrorInvalidValue;
   if (!make_chunk_map(&tk, p.k, p.D, p.Nkv, p.B * p.Hkv, BN, L::IC)) return cudaErrorInvalidValue;
   if (!make_chunk_map(&tv, p.v, p.D, p.Nkv, p.B * p.Hkv, BN, L::IC)) return cudaErrorInvalidValue;
   static std::atomic<int> attr_set[64];
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[device].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tcx_kernel<NX, SC>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    cudaError_t e = cudaFuncSetAttribute(attn_tcx_kernel<NX, SC, UN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
     attr_set[device].store(1, std::memory_order_release);
   }
@@ -792,7 +800,7 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   int f = fits[device].load(std::memory_order_relaxed);
   if (f == 0) {
     int nclusters = 0;
-    cudaError_t q = cudaOccupancyMaxActiveClusters(&nclusters, attn_tcx_kernel<NX, SC>, &cfg);
+    cudaError_t q = cudaOccupancyMaxActiveClusters(&nclusters, attn_tcx_kernel<NX, SC, UN>, &cfg);
     if (q != cudaSuccess) {
       cudaGetLastError();
       nclusters = 0;
@@ -801,7 +809,7 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
     fits[device].store(f, std::memory_order_relaxed);
   }
   if (f != 1) return cudaErrorNotSupported;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tcx_kernel<NX, SC>, tq, tk, tv, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tcx_kernel<NX, SC, UN>, tq, tk, tv, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -810,7 +818,7 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
 
 int tcx_slices(int D) {
   if (!tcx_supports(D)) return 0;
-  return D == 384 || D == 512 ? 2 : 4;
+  return D <= 512 ? 2 : 4;
 }
 
 bool tcx_supports(int D) {
@@ -818,15 +826,22 @@ bool tcx_supports(int D) {
   (void)D;
   return false;
 #else
-  return D == 384 || D == 512 || D == 768 || D == 1024;
+  // from D = 384: at D = 320 the per-slice kernel measured faster (578 against
+  // 540 TFLOP/s on B1 H8 N4096), at 448 the two tie
+  return D % 64 == 0 && D >= 384 && D <= 1024;
 #endif
 }
 
 cudaError_t launch_tcx(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
-  if (p.D == 384) return launch_tcx_n<2, 3>(p, device, wait_limit_ns, stream);
-  if (p.D == 512) return launch_tcx_n<2, 4>(p, device, wait_limit_ns, stream);
-  if (p.D == 768) return launch_tcx_n<4, 3>(p, device, wait_limit_ns, stream);
-  if (p.D == 1024) return launch_tcx_n<4, 4>(p, device, wait_limit_ns, stream);
+  if (p.D == 384) return launch_tcx_n<2, 3, false>(p, device, wait_limit_ns, stream);
+  if (p.D == 512) return launch_tcx_n<2, 4, false>(p, device, wait_limit_ns, stream);
+  if (p.D == 768) return launch_tcx_n<4, 3, false>(p, device, wait_limit_ns, stream);
+  if (p.D == 1024) return launch_tcx_n<4, 4, false>(p, device, wait_limit_ns, stream);
+  // uneven slices: 2 CTAs up to D = 512, 4 above, at most four chunks each
+  const int nc = p.D / 64;
+  if (nc == 7) return launch_tcx_n<2, 4, true>(p, device, wait_limit_ns, stream);
+  if (nc >= 9 && nc <= 11) return launch_tcx_n<4, 3, true>(p, device, wait_limit_ns, stream);
+  if (nc >= 13 && nc <= 15) return launch_tcx_n<4, 4, true>(p, device, wait_limit_ns, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -210,7 +210,7 @@ ATTN_API int attn_fwd_status(attn_stream_t stream);
  *     in the status word, every role of the CTA stops waiting, drains its own
  *     copies and MMAs, frees its tensor memory and exits (no trap, no hang;
  *     outputs of that call are undefined);
- *   ATTN_DEBUG_NO_CLUSTER, which runs head dims 384, 512, 768 and 1024 on the
+ *   ATTN_DEBUG_NO_CLUSTER, which runs head dims 384 ... 1024 on the
  *     per-slice Split-D kernel (each output slice recomputes the scores)
  *     instead of the cluster kernel, the path a device takes when it cannot
  *     hold one cluster; results agree within the parity tolerances.

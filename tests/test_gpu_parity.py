@@ -35,7 +35,7 @@ def test_named_workload(name):
     assert mx <= 2e-2 and mean <= 2e-3 and dl <= 1e-3, (mx, mean, dl)
 
 
-@pytest.mark.parametrize("D", [64, 128, 192, 256, 320, 384, 448, 512, 640, 768, 1024])
+@pytest.mark.parametrize("D", [64, 128, 192, 256, 320, 384, 448, 512, 576, 640, 704, 768, 832, 896, 960, 1024])
 @pytest.mark.parametrize("causal", [False, True])
 def test_head_dims(D, causal):
     check_case(1, 2, 1, 200, 200, D, causal, seed=D + causal)
@@ -55,7 +55,7 @@ def test_gqa_ratios(Hq, Hkv, causal):
     check_case(2, Hq, Hkv, 300, 300, 128, causal, seed=Hq * 10 + Hkv)
 
 
-# D = 384, 512, 768 and 1024 run on clusters of 2 or 4 CTAs that exchange partial scores
+# D = 384 ... 1024 run on clusters of 2 or 4 CTAs that exchange partial scores
 # and P; these cases cover single-row and single-key problems, key counts
 # below one block, ragged tails, GQA, rows that see no key, and a negative
 # and a zero scale.
@@ -70,14 +70,14 @@ CLUSTER_CASES = [
 ]
 
 
-@pytest.mark.parametrize("D", [384, 512, 768, 1024])
+@pytest.mark.parametrize("D", [384, 448, 512, 640, 768, 896, 1024])
 @pytest.mark.parametrize("case", CLUSTER_CASES, ids=[str(c) for c in CLUSTER_CASES])
 def test_cluster_splitd_cases(D, case):
     B, Hq, Hkv, Nq, Nkv, causal, scale = case
     check_case(B, Hq, Hkv, Nq, Nkv, D, causal, seed=Nq + Nkv + D, scale=scale)
 
 
-@pytest.mark.parametrize("D", [384, 512, 768, 1024])
+@pytest.mark.parametrize("D", [384, 448, 512, 640, 768, 1024])
 @pytest.mark.parametrize("causal", [False, True])
 def test_per_slice_path(D, causal):
     # the path taken where a cluster does not fit: each output slice recomputes S
@@ -89,7 +89,7 @@ def test_per_slice_path(D, causal):
         attn_set_debug(0)
 
 
-@pytest.mark.parametrize("D", [384, 512, 768, 1024])
+@pytest.mark.parametrize("D", [384, 448, 512, 640, 768, 1024])
 def test_cluster_splitd_deterministic(D):
     q, k, v = (t.cuda() for t in make_qkv(1, 2, 2, 300, 500, D, 23))
     o1, l1 = attn_fwd(q, k, v, causal=True)
