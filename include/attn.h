@@ -87,6 +87,13 @@ typedef struct CUstream_st *attn_stream_t;
  * tiles to fill the GPU.  Bounded device-side waits that run out are not
  * reported here: call attn_fwd_status.
  *
+ * CUDA graphs: the call keeps no state between calls that a graph replay
+ * would miss (the tensor maps are kernel parameters, the workspace is
+ * stream-ordered), so it may be captured into a graph once the same sizes
+ * have run outside capture on that device (the first call of a size does
+ * one-time set-up that capture forbids: device facts, kernel attributes, the
+ * cluster-fit query).  A replay reads and writes the captured pointers.
+ *
  * Returns ATTN_OK or a negative ATTN_ERR_* code; on error nothing is launched.
  */
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
