@@ -98,6 +98,26 @@ def test_cluster_splitd_deterministic(D):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+# large and lopsided shapes: one query against 128 Ki keys (automatic key
+# splits), few queries against long keys on the cluster kernel, a grid of
+# 4096 (b, hq) heads, causal cross-attention with Nkv far above Nq, and a
+# 32 Ki causal self-attention (rows sampled).
+LARGE_CASES = [
+    (1, 8, 1, 1, 131072, 128, False, 0),
+    (1, 4, 2, 64, 65536, 512, False, 0),
+    (256, 16, 16, 128, 128, 64, True, 0),
+    (1, 4, 4, 1000, 9000, 128, True, 0),
+    (1, 2, 2, 1000, 9000, 768, True, 0),
+    (1, 2, 1, 32768, 32768, 128, True, 256),
+]
+
+
+@pytest.mark.parametrize("case", LARGE_CASES, ids=[str(c) for c in LARGE_CASES])
+def test_large_shapes(case):
+    B, Hq, Hkv, Nq, Nkv, D, causal, nrows = case
+    check_case(B, Hq, Hkv, Nq, Nkv, D, causal, seed=Nq + Nkv + D, nrows=nrows)
+
+
 @pytest.mark.parametrize("D", [128, 512])
 def test_large_scores(D):
     # scale 1 on amp-2 inputs: scores of order 2*sqrt(D)*2; stresses the running max
