@@ -382,12 +382,66 @@ def _mutant(kind):
                     O[b, h] = np.where(live[:, None], acc / l1[:, None], 0)
                     L[b, h] = np.where(live, np.where(live, m, 0) + np.log(l1), -np.inf)
             return O, L
+        if kind in ("causal_strict", "causal_shift_sign", "lse_log2", "lse_unscaled", "pv_uses_k", "gqa_div_hkv"):
+            return _variant(kind, q, k, v, scale, causal)
         raise ValueError(kind)
     return fn
 
 
+def _variant(kind, q, k, v, scale, causal):
+    """The definition written out once more with one deliberate slip."""
+    B, Hq, Nq, _ = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    O = np.zeros((B, Hq, Nq, v.shape[3]))
+    L = np.zeros((B, Hq, Nq))
+    i = np.arange(Nq)[:, None]
+    j = np.arange(Nkv)[None]
+    for b in range(B):
+        for h in range(Hq):
+            kv = min(h // Hkv, Hkv - 1) if kind == "gqa_div_hkv" else h // (Hq // Hkv)
+            raw = q[b, h] @ k[b, kv].T
+            S = scale * raw
+            if causal:
+                if kind == "causal_strict":
+                    vis = j < i + (Nkv - Nq)            # the diagonal masked too
+                elif kind == "causal_shift_sign":
+                    vis = j <= i - (Nkv - Nq)           # offset with the wrong sign
+                else:
+                    vis = j <= i + (Nkv - Nq)
+                S = np.where(vis, S, -np.inf)
+                raw = np.where(vis, raw, -np.inf)
+            m = S.max(1) if Nkv else np.full(Nq, -np.inf)
+            live = np.isfinite(m)
+            m0 = np.where(live, m, 0.0)
+            E = np.exp(S - m0[:, None])
+            l1 = np.where(live, E.sum(1), 1.0)
+            src = k[b, kv] if kind == "pv_uses_k" else v[b, kv]
+            O[b, h] = np.where(live[:, None], E @ src / l1[:, None], 0.0)
+            if kind == "lse_log2":
+                L[b, h] = np.where(live, (m0 + np.log(l1)) / math.log(2.0), -np.inf)
+            elif kind == "lse_unscaled":
+                mr = np.where(live, raw.max(1), 0.0)
+                L[b, h] = np.where(live, mr + np.log(np.exp(raw - mr[:, None]).sum(1)), -np.inf)
+            else:
+                L[b, h] = np.where(live, m0 + np.log(l1), -np.inf)
+    return O, L
+
+
 MUTANTS = ["no_scale", "scale_squared", "gqa_modulo", "causal_topleft", "lse_no_max", "unnormalised",
-           "transposed_pv", "online_sign"]
+           "transposed_pv", "online_sign", "causal_strict", "causal_shift_sign", "lse_log2", "lse_unscaled",
+           "pv_uses_k", "gqa_div_hkv"]
+
+
+def test_variant_without_slip_matches_oracle():
+    # the helper that plants the slips is itself the definition when no slip is chosen
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((2, 4, 9, 8))
+    k = rng.standard_normal((2, 2, 13, 8))
+    v = rng.standard_normal((2, 2, 13, 8))
+    for causal in (False, True):
+        O, L = _variant("none", q, k, v, 0.3, causal)
+        O_ref, L_ref = oracle.attention(q, k, v, 0.3, causal)
+        assert np.allclose(O, O_ref, atol=1e-12) and np.allclose(L, L_ref, atol=1e-12)
 
 
 @pytest.mark.parametrize("kind", MUTANTS)
