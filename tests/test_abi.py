@@ -129,3 +129,21 @@ def test_missing_library_fails_loudly(tmp_path):
     env = dict(os.environ, ATTN_GB300_LIB=str(tmp_path / "nope.so"), PYTHONPATH=ROOT)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
     assert "RAISED" in r.stdout and "no fallback" in r.stdout
+
+
+def test_plain_c_client(lib, tmp_path):
+    # the C ABI from plain C: header + shared library, no C++ and no torch
+    import shutil
+    import torch
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(lib._name)
+    exe = str(tmp_path / "attn_client")
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c_client", "attn_client.c"), "-L", libdir, "-lattn_gb300",
+                        f"-Wl,-rpath,{libdir}", "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    args = [] if torch.cuda.is_available() else ["--no-device"]
+    r = subprocess.run([exe] + args, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "OK" in r.stdout, r.stdout + r.stderr
