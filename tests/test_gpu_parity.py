@@ -118,6 +118,26 @@ def test_large_shapes(case):
     check_case(B, Hq, Hkv, Nq, Nkv, D, causal, seed=Nq + Nkv + D, nrows=nrows)
 
 
+@pytest.mark.parametrize("scale", [-0.09, 0.0])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128, 192, 256, 320])
+def test_nonpositive_scale(D, causal, scale):
+    # scale <= 0 runs the kernels' other instantiation (block minimum of the
+    # raw scores instead of the maximum); scale 0 gives uniform weights
+    check_case(1, 4, 2, 300, 333, D, causal, seed=D + 17 * causal, scale=scale)
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0])
+def test_nonpositive_scale_splitkv(scale):
+    q, k, v = make_qkv(1, 2, 1, 200, 1500, 128, seed=9)
+    out = torch.full((1, 2, 200, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((1, 2, 200), float("nan"), dtype=torch.float32, device="cuda")
+    attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=True, out=out, lse=lse, kv_splits=3)
+    torch.cuda.synchronize()
+    mx, mean, dl = compare(out.cpu(), lse.cpu(), q, k, v, scale, True)
+    assert mx <= 2e-2 and mean <= 2e-3 and dl <= 1e-3, (mx, mean, dl)
+
+
 @pytest.mark.parametrize("D", [128, 512])
 def test_large_scores(D):
     # scale 1 on amp-2 inputs: scores of order 2*sqrt(D)*2; stresses the running max
