@@ -216,6 +216,9 @@ SPLIT_CASES = [
     (1, 1, 1, 100, 900, 192, False),
     (1, 2, 2, 150, 600, 512, True),
     (1, 1, 1, 128, 700, 1024, False),
+    (1, 2, 1, 150, 700, 448, True),     # cluster kernel, uneven slices (4 + 3 chunks)
+    (1, 2, 2, 200, 600, 640, False),    # uneven slices over four CTAs
+    (1, 1, 1, 128, 900, 896, False),
     (1, 2, 1, 300, 100, 128, True),     # causal, Nq > Nkv: fully masked rows in every range
 ]
 
