@@ -136,14 +136,41 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(src: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed, so
+    that an edit of comments or layout alone leaves the hash unchanged.
+    String and character literals are kept whole."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """First 16 hex digits of sha256 over the named kernel's source files."""
+    """First 16 hex digits of sha256 over the code (comments and layout
+    removed) of the named kernel's source files."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_attn_gb300", "csrc")
     for f in sorted(KERNEL_SOURCES[kernel]):
-        with open(os.path.join(csrc, f), "rb") as fh:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(f.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -151,7 +151,7 @@ void make_plan(const Problem &p, const DeviceInfo &dev, int splits, attn_plan *p
 }
 
 // The tensor-core kernel for the head dim: two-tile (D 64, 128), cluster
-// Split-D (D 512, 1024), else the Split-D kernel with per-slice scores.
+// Split-D (D 384 ... 1024), else the Split-D kernel with per-slice scores.
 cudaError_t launch_tensor(const Problem &p, int device, cudaStream_t st) {
   if (tc2_supports(p.D)) return launch_tc2(p, device, wait_limit_ns(), st);
   if (tcx_supports(p.D) && !(debug_flags() & ATTN_DEBUG_NO_CLUSTER)) {
