@@ -24,6 +24,16 @@ What is computed (the plain definition; sources by page title and section):
 * "ZYFA: FP8 FlashAttention Kernels for AMD MI355X", section "The details that
   make it production-grade": log-sum-exp values let results computed over
   disjoint key ranges be merged.
+* "ffpa-attn 0.2.3" README feature table ("Causal/Mask"): an attention mask
+  besides the causal one.  Read here as SDPA's additive float mask: it is
+  added to the scaled scores before the row maximum, and an entry of -inf
+  hides that key from that query.
+* "FlashAttention v1/v2/v3/v4", section "FA1 -- el cambio de orden de las
+  operaciones", and the "FlashAttention: Fast and Memory-Efficient Exact
+  Attention with IO-Awareness" summary card: the backward pass keeps only the
+  row statistics and recomputes S from Q and K.  What it computes is the
+  gradient of the forward definition; ``attention_backward`` writes that
+  gradient out (chain rule through the row softmax, below).
 
 Readings where the pages are silent (each is listed with the others in the
 design notes):
@@ -37,6 +47,9 @@ design notes):
 4. GQA groups are consecutive: query head hq reads key/value head
    hq // (Hq / Hkv).
 5. scale is an explicit argument (the workloads use 1/sqrt(D)).
+6. The additive mask M (any array that broadcasts to [B, Hq, Nq, Nkv]) enters
+   as S = scale * Q K^T + M, then the causal mask; finite entries and -inf
+   are allowed.  A row whose every entry ends up -inf is reading 3's row.
 
 Parity status: pinned (see tests/test_oracle.py): brute force on tiny inputs,
 torch's float64 scaled_dot_product_attention, closed forms and invariants.
@@ -69,20 +82,24 @@ def causal_visible(rows: np.ndarray, Nq: int, Nkv: int) -> np.ndarray:
 # the plain definition, one head at a time
 
 def scores_head(q: np.ndarray, k: np.ndarray, scale: float, causal: bool,
-                rows: np.ndarray | None = None) -> np.ndarray:
-    """S = scale * Q K^T for the chosen query rows, masked entries -inf."""
+                rows: np.ndarray | None = None, mask: np.ndarray | None = None) -> np.ndarray:
+    """S = scale * Q K^T (+ mask) for the chosen query rows, masked entries -inf.
+    ``mask`` is this head's additive mask, broadcastable to [Nq, Nkv] (all
+    rows; the chosen ones are taken from it)."""
     Nq, Nkv = q.shape[0], k.shape[0]
     rows = np.arange(Nq) if rows is None else np.asarray(rows, dtype=np.int64)
     S = scale * (q[rows] @ k.T)
+    if mask is not None:
+        S = S + np.broadcast_to(np.asarray(mask, dtype=np.float64), (Nq, Nkv))[rows]
     if causal:
         S = np.where(causal_visible(rows, Nq, Nkv), S, -np.inf)
     return S
 
 
-def probs_head(q, k, scale, causal, rows=None) -> np.ndarray:
+def probs_head(q, k, scale, causal, rows=None, mask=None) -> np.ndarray:
     """Row softmax of the masked scores: P[i, j] = exp(S_ij - m_i) / l_i.
     Rows with no visible key are all zero."""
-    S = scores_head(q, k, scale, causal, rows)
+    S = scores_head(q, k, scale, causal, rows, mask)
     m = S.max(axis=1) if S.shape[1] else np.full(S.shape[0], -np.inf)
     live = np.isfinite(m)
     m0 = np.where(live, m, 0.0)
@@ -92,14 +109,14 @@ def probs_head(q, k, scale, causal, rows=None) -> np.ndarray:
 
 
 def attention_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
-                   causal: bool, rows: np.ndarray | None = None):
+                   causal: bool, rows: np.ndarray | None = None, mask: np.ndarray | None = None):
     """One head.  q [Nq, D], k and v [Nkv, D], float64.
 
     Returns (O [r, D], LSE [r]) for the r chosen query rows:
     m_i = max_j S_ij, l_i = sum_j exp(S_ij - m_i), O_i = sum_j exp(S_ij - m_i) v_j / l_i,
     LSE_i = m_i + ln l_i.
     """
-    S = scores_head(q, k, scale, causal, rows)
+    S = scores_head(q, k, scale, causal, rows, mask)
     r = S.shape[0]
     if S.shape[1] == 0:
         return np.zeros((r, v.shape[1])), np.full(r, -np.inf)
@@ -115,8 +132,9 @@ def attention_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
 
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool,
-              rows: np.ndarray | None = None):
-    """Batched oracle.  q [B, Hq, Nq, D], k and v [B, Hkv, Nkv, D] (float64).
+              rows: np.ndarray | None = None, mask: np.ndarray | None = None):
+    """Batched oracle.  q [B, Hq, Nq, D], k and v [B, Hkv, Nkv, D] (float64);
+    mask (optional) broadcastable to [B, Hq, Nq, Nkv].
 
     Returns O [B, Hq, r, D] and LSE [B, Hq, r] (r = Nq, or len(rows) when a
     row subset is given; the same rows are used for every head).
@@ -129,25 +147,30 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal:
     if Bk != B or Dk != D or v.shape[:3] != k.shape[:3]:
         raise ValueError("shape mismatch")
     r = Nq if rows is None else len(rows)
+    M = None if mask is None else np.broadcast_to(np.asarray(mask, dtype=np.float64), (B, Hq, Nq, Nkv))
     O = np.zeros((B, Hq, r, v.shape[3]))
     LSE = np.zeros((B, Hq, r))
     for b in range(B):
         for h in range(Hq):
             kv = kv_head_of(h, Hq, Hkv)
-            O[b, h], LSE[b, h] = attention_head(q[b, h], k[b, kv], v[b, kv], scale, causal, rows)
+            O[b, h], LSE[b, h] = attention_head(q[b, h], k[b, kv], v[b, kv], scale, causal, rows,
+                                                None if M is None else M[b, h])
     return O, LSE
 
 
 # ---------------------------------------------------------------------------
 # brute force, pure-Python loops (tiny inputs only)
 
-def attention_bruteforce(q, k, v, scale, causal):
-    """Same definition with explicit loops and math.exp; for N, D <= ~16."""
+def attention_bruteforce(q, k, v, scale, causal, mask=None):
+    """Same definition with explicit loops and math.exp; for N, D <= ~16.
+    ``mask`` (optional) broadcasts to [B, Hq, Nq, Nkv] and is added to each
+    scaled score; a -inf entry drops the key."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     B, Hq, Nq, D = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
+    M = None if mask is None else np.broadcast_to(np.asarray(mask, dtype=np.float64), (B, Hq, Nq, Nkv))
     group = Hq // Hkv
     O = np.zeros((B, Hq, Nq, v.shape[3]))
     LSE = np.zeros((B, Hq, Nq))
@@ -162,7 +185,12 @@ def attention_bruteforce(q, k, v, scale, causal):
                     dot = 0.0
                     for d in range(D):
                         dot += float(q[b, h, i, d]) * float(k[b, kh, j, d])
-                    s.append((j, scale * dot))
+                    x = scale * dot
+                    if M is not None:
+                        if M[b, h, i, j] == -math.inf:
+                            continue
+                        x += float(M[b, h, i, j])
+                    s.append((j, x))
                 if not s:
                     LSE[b, h, i] = -math.inf
                     continue
@@ -235,3 +263,55 @@ def lse_merge(parts):
     LSE = np.where(live, mx0 + np.log(tot1), -np.inf)
     O = np.where(live[:, None], (w[:, :, None] * Os).sum(axis=0) / tot1[:, None], 0.0)
     return O, LSE
+
+
+# ---------------------------------------------------------------------------
+# backward: the gradient of the forward definition
+
+def attention_backward_head(q, k, v, do, scale, causal, mask=None):
+    """Gradients of one head's O with respect to q, k and v, given the
+    upstream gradient dO [Nq, Dv] of the output.
+
+    With P the row softmax of S = scale * Q K^T (+ mask, causal -inf) and
+    O = P V, the chain rule through the row softmax gives
+        dV = P^T dO
+        dP = dO V^T
+        Delta_i = sum_j P_ij dP_ij  (= sum_d dO_id O_id)
+        dS = P * (dP - Delta)        (elementwise, Delta broadcast over j)
+        dQ = scale * dS K,   dK = scale * dS^T Q.
+    Masked entries have P = 0 and receive no gradient; rows with no visible
+    key contribute nothing.  Returns (dq [Nq, D], dk [Nkv, D], dv [Nkv, Dv]).
+    """
+    P = probs_head(q, k, scale, causal, None, mask)
+    O = P @ v
+    dV = P.T @ do
+    dP = do @ v.T
+    delta = (do * O).sum(axis=1)
+    dS = P * (dP - delta[:, None])
+    return scale * (dS @ k), scale * (dS.T @ q), dV
+
+
+def attention_backward(q, k, v, do, scale, causal, mask=None):
+    """Batched gradients: q and do [B, Hq, Nq, D], k and v [B, Hkv, Nkv, D],
+    mask (optional) broadcastable to [B, Hq, Nq, Nkv].  A key/value head
+    shared by a GQA group of query heads receives the sum of their gradients.
+    Returns (dq, dk, dv) in float64 with the shapes of q, k and v."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    B, Hq, Nq, D = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    M = None if mask is None else np.broadcast_to(np.asarray(mask, dtype=np.float64), (B, Hq, Nq, Nkv))
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            kv = kv_head_of(h, Hq, Hkv)
+            gq, gk, gv = attention_backward_head(q[b, h], k[b, kv], v[b, kv], do[b, h], scale, causal,
+                                                 None if M is None else M[b, h])
+            dq[b, h] = gq
+            dk[b, kv] += gk
+            dv[b, kv] += gv
+    return dq, dk, dv
