@@ -37,7 +37,8 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from exact_attention_attn_gb300.workloads import BENCH_WORKLOAD, WORKLOADS, make_workload_inputs, to_f64  # noqa: E402
+from exact_attention_attn_gb300.workloads import (BENCH_WORKLOAD, WORKLOADS, make_workload_inputs,  # noqa: E402
+                                                  sample_rows, to_f64)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
@@ -213,15 +214,28 @@ def blas_threads():
         return None
 
 
+def oracle_rows(w):
+    """Query rows the CPU oracle runs per head: the workload's seeded sample
+    (256 rows per head on the large workloads, the rows its parity checks
+    use), else every row."""
+    return sample_rows(w.Nq, w.sample_rows, w.seed) if w.sample_rows else None
+
+
 def time_oracle(w, q, k, v, budget_s: float, max_heads: int | None = None):
-    """Run the oracle head by head over the workload until budget_s seconds
-    have passed (at least one head).  Returns (TFLOPS, heads, seconds)."""
+    """Run the oracle head by head over the workload (on each head's sampled
+    rows where the workload samples) until budget_s seconds have passed (at
+    least one head).  Returns (TFLOPS, heads, seconds, rows per head).  The
+    FLOPs credited to a head are the workload's FLOPs per head times the
+    share of its rows that ran (a per-row linear extrapolation when rows are
+    sampled)."""
     import oracle
     B, Hq = w.B, w.Hq
     heads = [(b, h) for b in range(B) for h in range(Hq)]
     if max_heads:
         heads = heads[:max_heads]
-    per_head_flops = w.flops() / (B * Hq)
+    rows = oracle_rows(w)
+    nrows = w.Nq if rows is None else len(rows)
+    per_head_flops = w.flops() / (B * Hq) * nrows / w.Nq
     done = 0
     t0 = time.perf_counter()
     group = w.Hq // w.Hkv
@@ -229,12 +243,49 @@ def time_oracle(w, q, k, v, budget_s: float, max_heads: int | None = None):
         qh = to_f64(q[b, h])
         kh = to_f64(k[b, h // group])
         vh = to_f64(v[b, h // group])
-        oracle.attention_head(qh, kh, vh, w.scale, w.causal)
+        oracle.attention_head(qh, kh, vh, w.scale, w.causal, rows)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return per_head_flops * done / dt / 1e12, done, dt
+    return per_head_flops * done / dt / 1e12, done, dt, nrows
+
+
+def oracle_sample_text(w, heads, dt, nrows, threads):
+    what = (f"{nrows} seeded rows of each of {heads} (b,hq) heads (of {w.B * w.Hq}) of {w.name}; TFLOPS credit "
+            f"each head with its FLOPs x {nrows}/{w.Nq} (per-row linear extrapolation)" if nrows < w.Nq else
+            f"{heads} of {w.B * w.Hq} (b,hq) heads of {w.name}, all {w.Nq} rows each")
+    return f"{what}; float64 numpy on {threads} host thread(s), {dt:.1f} s"
+
+
+def single_thread_oracle(w, budget_s: float):
+    """The oracle on one host thread, in a child process whose BLAS pools are
+    capped at one thread before numpy loads.  Returns the cpu_baseline-style
+    dict, or None if the child fails."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-only", "--workload", w.name,
+           "--cpu-seconds", str(budget_s)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s * 4 + 120)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+    except (subprocess.TimeoutExpired, ValueError, IndexError):
+        return None
+
+
+def oracle_only(args, w):
+    q, k, v = make_workload_inputs(w)
+    tf, heads, dt, nrows = time_oracle(w, q, k, v, budget_s=args.cpu_seconds)
+    threads = blas_threads() or int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0) or cpu_cores()
+    print(json.dumps({"value": tf, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                      "sample": oracle_sample_text(w, heads, dt, nrows, threads)}), flush=True)
+    return 0
+
+
+def bench_config(w, ws: int) -> dict:
+    """The workload as both arms report it."""
+    return dict(w.describe(), l2="flushed between steps (512 MiB write, outside the events)",
+                parallelism=f"replicas x{ws}" if ws > 1 else "1 GPU")
 
 
 # --------------------------------------------------------------------------
@@ -247,22 +298,22 @@ def run_reference(args, w):
     per_step_budget = 5.0
     for _ in range(args.warmup):
         time_oracle(w, q, k, v, budget_s=0.0, max_heads=1)
-    vals, heads_total, secs = [], 0, 0.0
+    vals, heads_total, secs, nrows = [], 0, 0.0, w.Nq
     for _ in range(args.steps):
-        tf, heads, dt = time_oracle(w, q, k, v, budget_s=per_step_budget)
+        tf, heads, dt, nrows = time_oracle(w, q, k, v, budget_s=per_step_budget)
         vals.append(tf)
         heads_total += heads
         secs += dt
     value = statistics.mean(vals)
     cores = blas_threads() or cpu_cores()
-    sample = (f"{heads_total} (b,hq) heads of {w.name} in total over {args.steps} steps, all {w.Nq} query rows each, "
-              f"float64 numpy on the host; each step stops after {per_step_budget:.0f} s")
+    sample = (oracle_sample_text(w, heads_total, secs, nrows, cores) +
+              f"; {args.steps} steps, each stopping after {per_step_budget:.0f} s")
     flops_per_head = w.flops() / (w.B * w.Hq)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 0 if ws <= 1 else ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(w.describe(), l2="n/a (host)"),
+        "config": bench_config(w, ws),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "flops_per_head": flops_per_head,
@@ -327,15 +378,24 @@ def run_ours(args, w):
     flops = w.flops()
     value = flops * max(ws, 1) / (ms * 1e-3) / 1e12
 
-    # roofline of the dominant (here: the only) kernel of a step
+    # roofline of the dominant (here: the only) kernel of a step: the tensor
+    # pipe where the workload's FLOPs per algorithmic byte exceed the
+    # machine's ridge (peak FLOP/s / HBM B/s), else HBM
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     achieved = flops / (ms_local * 1e-3) / 1e12
+    achieved_gbs = w.hbm_bytes() / (ms_local * 1e-3) / 1e9
     traffic, traffic_kernel = recorded_traffic(w.name)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": traffic, "peak_source": f"{peak_src} bf16 dense burst",
-                "algorithmic_flops_per_launch": flops, "algorithmic_hbm_bytes_per_launch": w.hbm_bytes(),
-                "achieved_hbm_gbs": w.hbm_bytes() / (ms_local * 1e-3) / 1e9,
-                "kernel": traffic_kernel}
+    common = {"traffic": traffic, "algorithmic_flops_per_launch": flops, "algorithmic_hbm_bytes_per_launch": w.hbm_bytes(),
+              "kernel": traffic_kernel}
+    if flops / w.hbm_bytes() > peak * 1e3 / hbm_peak:
+        roofline = dict({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_src} bf16 dense burst",
+                         "achieved_hbm_gbs": achieved_gbs}, **common)
+    else:
+        roofline = dict({"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved_gbs / hbm_peak, "peak_source": f"{peak_src} HBM copy",
+                         "achieved_tflops": achieved, "us_per_launch": ms_local * 1e3}, **common)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -359,18 +419,19 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and ws <= 1 and not args.no_cpu_baseline:
-        tf, heads, dt = time_oracle(w, q, k, v, budget_s=args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOPS", "cores": blas_threads() or cpu_cores(), "kind": "oracle",
-               "sample": f"{heads} of {w.B * w.Hq} (b,hq) heads of {w.name}, all {w.Nq} rows each, "
-                         f"float64 numpy, {dt:.1f} s"}
+        tf, heads, dt, nrows = time_oracle(w, q, k, v, budget_s=args.cpu_seconds)
+        threads = blas_threads() or cpu_cores()
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+               "sample": oracle_sample_text(w, heads, dt, nrows, threads)}
+        if w.sample_rows == 0:  # the two small workloads: also on one host thread
+            cpu["single_thread"] = single_thread_oracle(w, args.cpu_seconds)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": max(ws, 1), "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(w.describe(), l2="flushed between steps (512 MiB write, outside the events)",
-                           parallelism=f"replicas x{max(ws, 1)}" if ws > 1 else "1 GPU"),
+            "config": bench_config(w, ws),
             "pct_of_peak": 100.0 * value / max(ws, 1) / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * kernels_per_call(w),
@@ -398,10 +459,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    w = WORKLOADS[args.workload]
+    if args.oracle_only:  # the single-thread CPU leg's child process
+        return oracle_only(args, w)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

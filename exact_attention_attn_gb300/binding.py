@@ -28,7 +28,7 @@ class AttnPlan(ctypes.Structure):
                 ("kv_splits", ctypes.c_int), ("d_slices", ctypes.c_int), ("workspace_bytes", ctypes.c_longlong)]
 
 
-PATH_NAMES = {0: "none", 1: "simt", 2: "tc", 3: "tc_splitkv"}
+PATH_NAMES = {0: "none", 1: "nokeys", 2: "tc", 3: "tc_splitkv"}
 
 
 class AttnError(RuntimeError):

@@ -82,8 +82,6 @@ int check_sizes(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal) {
   return ATTN_OK;
 }
 
-constexpr int kMaxSplits = 64;
-
 // CTAs of the tensor-core launch for one key range per query tile.
 // D-slices per 128-row tile: the cluster kernel's CTAs per cluster where it
 // runs, else the per-slice kernel's output slices.
@@ -130,10 +128,10 @@ void make_plan(const Problem &p, const DeviceInfo &dev, int splits, attn_plan *p
     return;
   }
   if (p.Nkv == 0) {  // no keys: every row is O = 0, LSE = -inf
-    plan->path = ATTN_PATH_SIMT;
+    plan->path = ATTN_PATH_NOKEYS;
     plan->launches = 1;
-    plan->d_slices = (p.D + 255) / 256;
-    plan->grid = (int)(((int64_t)(p.Nq + 63) / 64) * p.B * p.Hq * plan->d_slices);
+    const int64_t blocks = ((int64_t)p.B * p.Hq * p.Nq * (p.D / 8) + 255) / 256;
+    plan->grid = (int)(blocks < (int64_t)dev.sm_count * 8 ? (blocks < 1 ? 1 : blocks) : (int64_t)dev.sm_count * 8);
     return;
   }
   const int s = splits > 0 ? splits : auto_splits(p, dev.sm_count);
@@ -150,25 +148,14 @@ void make_plan(const Problem &p, const DeviceInfo &dev, int splits, attn_plan *p
   }
 }
 
-// The tensor-core kernel for the head dim: two-tile (D 64, 128), cluster
-// Split-D (D 384 ... 1024), else the Split-D kernel with per-slice scores.
-cudaError_t launch_tensor(const Problem &p, int device, cudaStream_t st) {
-  if (tc2_supports(p.D)) return launch_tc2(p, device, wait_limit_ns(), st);
-  if (tcx_supports(p.D) && !(debug_flags() & ATTN_DEBUG_NO_CLUSTER)) {
-    const cudaError_t e = launch_tcx(p, device, wait_limit_ns(), st);
-    if (e != cudaErrorNotSupported) return e;  // else no room for the cluster: per-slice kernel
-  }
-  return launch_tc(p, device, wait_limit_ns(), st);
-}
-
 int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   switch (plan.path) {
     case ATTN_PATH_NONE:
       return ATTN_OK;
-    case ATTN_PATH_SIMT:
+    case ATTN_PATH_NOKEYS:
       p.kv_splits = 1;
-      e = launch_simt(p, st);
+      e = launch_nokeys(p, dev.sm_count, st);
       break;
     case ATTN_PATH_TC:
       p.kv_splits = 1;
@@ -213,6 +200,17 @@ int current_device(int *device, int *sm_count, int **status) {
 }
 
 int record_cuda_error(cudaError_t e) { return record(e); }
+
+// The tensor-core kernel for the head dim: two-tile (D 64, 128), cluster
+// Split-D (D 384 ... 1024), else the Split-D kernel with per-slice scores.
+cudaError_t launch_tensor(const Problem &p, int device, cudaStream_t st) {
+  if (tc2_supports(p.D)) return launch_tc2(p, device, wait_limit_ns(), st);
+  if (tcx_supports(p.D) && !(debug_flags() & ATTN_DEBUG_NO_CLUSTER)) {
+    const cudaError_t e = launch_tcx(p, device, wait_limit_ns(), st);
+    if (e != cudaErrorNotSupported) return e;  // else no room for the cluster: per-slice kernel
+  }
+  return launch_tc(p, device, wait_limit_ns(), st);
+}
 
 int check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal) {
   return check_sizes(B, Hq, Hkv, Nq, Nkv, D, causal);

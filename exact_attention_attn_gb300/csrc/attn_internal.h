@@ -95,8 +95,17 @@ int record_cuda_error(cudaError_t e);
 // The size and flag checks of attn_fwd (ATTN_OK or ATTN_ERR_ARG), no device work.
 int check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int causal);
 
-// Plain CUDA-core kernel: correct for every supported shape; used for the
-// shapes the tensor-core kernel does not take.
-cudaError_t launch_simt(const Problem &p, cudaStream_t stream);
+// Problems with no keys: O = 0 and LSE = -inf everywhere (grid of at most
+// 8 CTAs per SM, grid-stride).
+cudaError_t launch_nokeys(const Problem &p, int sm_count, cudaStream_t stream);
+
+// Most key-range splits attn_fwd_splitkv accepts.
+constexpr int kMaxSplits = 64;
+
+// The tensor-core kernel for the head dim, as attn_fwd picks it: two-tile
+// (D 64, 128), cluster Split-D (D 384 ... 1024, unless ATTN_DEBUG_NO_CLUSTER
+// is set or the device cannot hold one cluster), else the per-slice kernel.
+// p.kv_splits > 1 writes the partials to p.ws_o / p.ws_lse.
+cudaError_t launch_tensor(const Problem &p, int device, cudaStream_t stream);
 
 }  // namespace attn

@@ -47,12 +47,10 @@ extern "C" int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void
                                         int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                                         float scale, int causal, int kv_splits, attn_stream_t stream) {
   using namespace attn;
-  if (B < 0 || Nq < 0 || Nkv < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_ARG;
-  if (D < 64 || D > ATTN_MAX_HEAD_DIM || D % 64 != 0) return ATTN_ERR_ARG;
-  if (causal != 0 && causal != 1) return ATTN_ERR_ARG;
-  if ((int64_t)B * Hq * Nq * (int64_t)D > (int64_t)1 << 46) return ATTN_ERR_ARG;
-  if ((int64_t)B * Hkv * Nkv * (int64_t)D > (int64_t)1 << 46) return ATTN_ERR_ARG;
-  if (!isfinite(scale) || kv_splits < 2 || kv_splits > 64) return ATTN_ERR_ARG;
+  // the size and flag checks of attn_fwd, then this entry point's own
+  int rc = check_problem(B, Hq, Hkv, Nq, Nkv, D, causal);
+  if (rc != ATTN_OK) return rc;
+  if (!isfinite(scale) || kv_splits < 2 || kv_splits > kMaxSplits) return ATTN_ERR_ARG;
   if (B == 0 || Nq == 0) return ATTN_OK;
   if (!q || !o || !lse) return ATTN_ERR_ARG;
   if (Nkv > 0 && (!k || !v)) return ATTN_ERR_ARG;
@@ -64,7 +62,7 @@ extern "C" int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void
 
   int device = 0, sm_count = 0;
   int *status = nullptr;
-  int rc = current_device(&device, &sm_count, &status);
+  rc = current_device(&device, &sm_count, &status);
   if (rc != ATTN_OK) return rc;
 
   Problem p{};
@@ -78,11 +76,12 @@ extern "C" int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void
   p.causal = causal;
   p.status = status;
   p.kv_splits = 1;
+  p.debug_flags = debug_flags();
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   cudaError_t e;
   if (Nkv == 0) {
-    e = launch_simt(p, st);
+    e = launch_nokeys(p, sm_count, st);
     return e == cudaSuccess ? ATTN_OK : record_cuda_error(e);
   }
   float *scratch = nullptr;
@@ -91,15 +90,8 @@ extern "C" int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void
   p.kv_splits = kv_splits;
   p.ws_o = scratch;
   p.ws_lse = scratch + (int64_t)kv_splits * rows * D;  // 16-byte aligned: D is a multiple of 64
-  const uint64_t limit = 2000000000ull;  // the same 2 s bound on device-side waits as attn_fwd
-  if (tc2_supports(D)) {
-    e = launch_tc2(p, device, limit, st);
-  } else {
-    // the cluster kernel where it fits on the device, else the per-slice one
-    e = tcx_supports(D) && !(debug_flags() & ATTN_DEBUG_NO_CLUSTER) ? launch_tcx(p, device, limit, st)
-                                                                  : cudaErrorNotSupported;
-    if (e == cudaErrorNotSupported) e = launch_tc(p, device, limit, st);
-  }
+  // the kernel choice, wait bound and debug flags of attn_fwd_splitkv
+  e = launch_tensor(p, device, st);
   if (e == cudaSuccess) e = launch_combine(p, st);
   return e == cudaSuccess ? ATTN_OK : record_cuda_error(e);
 }

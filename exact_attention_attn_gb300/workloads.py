@@ -77,7 +77,8 @@ WORKLOADS = {
                                                         1024, False, 4, amp=0.5, sample_rows=256),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
-BENCH_WORKLOAD = "causal_b4_h16_n2048_d128"
+# The bench's default: the largest workload (GQA causal N8192, 1.1 TFLOP per call)
+BENCH_WORKLOAD = "gqa_causal_b2_hq32_hkv8_n8192_d128"
 
 
 def make_qkv(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int, seed: int, amp: float = 1.0):

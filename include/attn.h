@@ -174,8 +174,9 @@ ATTN_API int attn_fwd_host(const void *q, const void *k, const void *v, void *o,
  * fixed, file-scope device array of ATTN_NOALLOC_SCRATCH_BYTES bytes that
  * every GPU which loads this library holds until the process exits.
  *
- * Arguments are those of attn_fwd_splitkv except that kv_splits must be an
- * explicit count from 2 to 64 (ATTN_ERR_ARG otherwise).  The partials need
+ * Arguments, checks, kernels, the device-side wait bound and the debug flags
+ * of attn_set_debug are those of attn_fwd_splitkv, except that kv_splits must
+ * be an explicit count from 2 to 64 (ATTN_ERR_ARG otherwise).  The partials need
  * kv_splits * B * Hq * Nq * (D + 1) * 4 bytes; a larger problem is refused
  * with ATTN_ERR_SCRATCH before anything is launched.  Nkv == 0 needs no
  * partials and runs the plain no-key path.
@@ -183,7 +184,9 @@ ATTN_API int attn_fwd_host(const void *q, const void *k, const void *v, void *o,
  * Set-up: the first call on a device looks up the array's device address
  * with cudaGetSymbolAddress (with that device current); make that first call
  * outside any stream capture.  No call of this function allocates or frees
- * device memory.
+ * device memory.  The address is kept for the life of the process, like the
+ * library's other per-device facts: do not call the library on a device
+ * again after cudaDeviceReset has destroyed its context.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents.  Nothing in it has to start at zero -- each call writes
@@ -243,7 +246,7 @@ ATTN_API const char *attn_last_cuda_error(void);
  * returns a negative ATTN_ERR_* code.
  */
 #define ATTN_PATH_NONE 0      /* empty problem: nothing is launched */
-#define ATTN_PATH_SIMT 1      /* CUDA-core kernel */
+#define ATTN_PATH_NOKEYS 1    /* no keys (Nkv == 0): a fill kernel writes O = 0, LSE = -inf */
 #define ATTN_PATH_TC 2        /* tcgen05 tensor-core kernel */
 #define ATTN_PATH_TC_SPLITKV 3 /* tcgen05 kernel over key splits + LSE merge kernel */
 

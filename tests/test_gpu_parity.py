@@ -158,6 +158,9 @@ def test_no_keys():
     k = torch.zeros((1, 1, 0, 128), dtype=torch.bfloat16)
     o, l = run_gpu(q, k, k.clone(), 0.1, False)
     assert torch.all(o == 0) and torch.all(torch.isneginf(l))
+    from exact_attention_attn_gb300 import attn_fwd_plan
+    plan = attn_fwd_plan(1, 2, 1, 70, 0, 128, False)
+    assert plan["path_name"] == "nokeys" and plan["launches"] == 1 and plan["grid"] >= 1
 
 
 def test_fully_masked_rows():
