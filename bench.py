@@ -129,7 +129,7 @@ class ClockSampler:
 
 # The sources a kernel's code and launch depend on: its own translation unit
 # plus the shared headers, the tensor-map builder and the launch planner.
-_COMMON_SOURCES = ("attn_internal.h", "sm100_ptx.cuh", "tma_host.cu", "attn_api.cu")
+_COMMON_SOURCES = ("attn_internal.h", "attn_mask.cuh", "sm100_ptx.cuh", "tma_host.cu", "attn_api.cu")
 KERNEL_SOURCES = {
     "attn_tc2_kernel": ("attn_tc2.cu",) + _COMMON_SOURCES,
     "attn_tc_kernel": ("attn_tc.cu",) + _COMMON_SOURCES,

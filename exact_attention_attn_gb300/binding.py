@@ -61,6 +61,9 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_splitkv.restype = ci
         lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
         lib.attn_fwd_splitkv_noalloc.restype = ci
+        ll = ctypes.c_longlong
+        lib.attn_fwd_masked.argtypes = [vp, vp, vp, vp, ll, ll, ll, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+        lib.attn_fwd_masked.restype = ci
         lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd_host.restype = ci
         lib.attn_set_debug.argtypes = [ci, ctypes.c_longlong]
@@ -108,15 +111,37 @@ def _check(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _mask_strides(mask: torch.Tensor, B: int, Hq: int, Nq: int, Nkv: int):
+    """Element strides (batch, head, query row) of a bf16 CUDA mask that
+    broadcasts to [B, Hq, Nq, Nkv] with contiguous keys; a broadcast or
+    size-1 dimension gets stride 0."""
+    if mask.dtype != torch.bfloat16:
+        raise TypeError(f"mask must be bfloat16, got {mask.dtype}")
+    if not mask.is_cuda:
+        raise ValueError("mask must be a CUDA tensor")
+    if mask.dim() > 4:
+        raise ValueError(f"mask must have at most 4 dims, got shape {tuple(mask.shape)}")
+    m = mask.reshape((1,) * (4 - mask.dim()) + tuple(mask.shape)).expand(B, Hq, Nq, Nkv)
+    if Nkv > 1 and m.stride(3) != 1:
+        raise ValueError("mask keys (last dim) must be contiguous")
+    strides = [0 if m.shape[d] == 1 else m.stride(d) for d in range(3)]
+    if any(st % 8 for st in strides) or m.data_ptr() % 16:
+        raise ValueError(f"mask strides {strides} must be multiples of 8 elements and its base 16-byte aligned "
+                         "(pad the key dimension to a multiple of 8)")
+    return m, strides
+
+
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
              causal: bool = False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-             stream=None, kv_splits: int | None = None):
+             stream=None, kv_splits: int | None = None, mask: torch.Tensor | None = None):
     """O, LSE = attention forward of bf16 q [B,Hq,Nq,D], k and v [B,Hkv,Nkv,D].
 
     O is bf16 [B,Hq,Nq,D]; LSE is fp32 [B,Hq,Nq] (natural log).  Runs
     asynchronously on ``stream`` (default: torch's current stream).
     ``kv_splits`` (None/0 = automatic) forces the number of key-range splits
-    (attn_fwd_splitkv).
+    (attn_fwd_splitkv).  ``mask`` (bf16, broadcastable to [B,Hq,Nq,Nkv],
+    keys contiguous) is an additive mask (attn_fwd_masked); it does not
+    combine with a forced ``kv_splits``.
     """
     lib = load_library()
     _check(q, "q", torch.bfloat16, 4)
@@ -137,7 +162,14 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | N
     if tuple(out.shape) != (B, Hq, Nq, D) or tuple(lse.shape) != (B, Hq, Nq):
         raise ValueError("out / lse shape mismatch")
     with torch.cuda.device(q.device):
-        if kv_splits:
+        if mask is not None:
+            if kv_splits:
+                raise ValueError("mask and kv_splits do not combine (attn_fwd_masked splits automatically)")
+            m, (sb, sh, sq) = _mask_strides(mask, B, Hq, Nq, Nkv)
+            rc = lib.attn_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), m.data_ptr(), sb, sh, sq,
+                                     out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq, Nkv, D, float(scale),
+                                     int(bool(causal)), _stream_handle(stream))
+        elif kv_splits:
             rc = lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                       B, Hq, Hkv, Nq, Nkv, D, float(scale), int(bool(causal)), int(kv_splits),
                                       _stream_handle(stream))

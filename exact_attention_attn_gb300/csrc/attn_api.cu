@@ -30,6 +30,10 @@ struct DeviceInfo {
   int sm_count = 0;
   int *status = nullptr;
   int device = 0;
+  // the split-KV workspace's memory pool: it keeps its memory between calls
+  // (the default pool hands memory back to the driver at every synchronise,
+  // and a fresh block from the driver costs more than the split saves)
+  cudaMemPool_t ws_pool = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -148,6 +152,36 @@ void make_plan(const Problem &p, const DeviceInfo &dev, int splits, attn_plan *p
   }
 }
 
+// Split-KV workspace on `st`: from the device's library pool (created on
+// first use, outside stream capture), or with cudaMallocAsync while `st` is
+// being captured into a graph (a graph memory node).
+cudaError_t workspace_alloc(const DeviceInfo &dev_c, void **ptr, size_t bytes, cudaStream_t st) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return e;
+  if (cap != cudaStreamCaptureStatusNone) return cudaMallocAsync(ptr, bytes, st);
+  DeviceInfo &dev = const_cast<DeviceInfo &>(dev_c);
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!dev.ws_pool) {
+      cudaMemPoolProps props;
+      memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev.device;
+      cudaMemPool_t pool = nullptr;
+      if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return e;
+      uint64_t keep = ~0ull;
+      if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+        cudaMemPoolDestroy(pool);
+        return e;
+      }
+      dev.ws_pool = pool;
+    }
+  }
+  return cudaMallocFromPoolAsync(ptr, bytes, dev.ws_pool, st);
+}
+
 int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   switch (plan.path) {
@@ -164,7 +198,7 @@ int launch_plan(Problem &p, const DeviceInfo &dev, const attn_plan &plan, cudaSt
     case ATTN_PATH_TC_SPLITKV: {
       // stream-ordered workspace: allocated and freed on the caller's stream
       void *ws = nullptr;
-      if (cudaMallocAsync(&ws, (size_t)plan.workspace_bytes, st) != cudaSuccess || !ws) {
+      if (workspace_alloc(dev, &ws, (size_t)plan.workspace_bytes, st) != cudaSuccess || !ws) {
         cudaGetLastError();
         return ATTN_ERR_NOMEM;
       }
@@ -250,10 +284,16 @@ int attn_set_debug(int flags, long long wait_limit_ns) {
   return ATTN_OK;
 }
 
-int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
-                     int B, int Hq, int Hkv, int Nq, int Nkv, int D,
-                     float scale, int causal, int kv_splits, attn_stream_t stream) {
-  using namespace attn;
+}  // extern "C"
+
+namespace attn {
+namespace {
+
+// attn_fwd_splitkv and attn_fwd_masked: checks, problem description, plan,
+// launch.  mask == nullptr: no additive mask.
+int fwd_common(const void *q, const void *k, const void *v, const void *mask, long long msb, long long msh,
+               long long msq, void *o, float *lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D, float scale,
+               int causal, int kv_splits, attn_stream_t stream) {
   int rc = check_sizes(B, Hq, Hkv, Nq, Nkv, D, causal);
   if (rc != ATTN_OK) return rc;
   if (!isfinite(scale) || kv_splits < 0 || kv_splits > kMaxSplits) return ATTN_ERR_ARG;
@@ -262,6 +302,7 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float
   if (Nkv > 0 && (!k || !v)) return ATTN_ERR_ARG;
   if (!aligned16(q) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
   if (Nkv > 0 && (!aligned16(k) || !aligned16(v))) return ATTN_ERR_ALIGN;
+  if (mask && Nkv > 0 && !aligned16(mask)) return ATTN_ERR_ALIGN;
 
   DeviceInfo *dev = nullptr;
   rc = device_info(&dev);
@@ -279,10 +320,38 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float
   p.status = dev->status;
   p.kv_splits = 1;
   p.debug_flags = debug_flags();
+  if (mask && Nkv > 0) {  // without keys the mask has nothing to act on
+    p.mask = static_cast<const __nv_bfloat16 *>(mask);
+    p.mask_sb = msb;
+    p.mask_sh = msh;
+    p.mask_sq = msq;
+  }
 
   attn_plan plan;
   make_plan(p, *dev, kv_splits, &plan);
   return launch_plan(p, *dev, plan, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                     float scale, int causal, int kv_splits, attn_stream_t stream) {
+  return attn::fwd_common(q, k, v, nullptr, 0, 0, 0, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal, kv_splits,
+                          stream);
+}
+
+int attn_fwd_masked(const void *q, const void *k, const void *v, const void *mask, long long mask_stride_b,
+                    long long mask_stride_h, long long mask_stride_q, void *o, float *lse, int B, int Hq, int Hkv,
+                    int Nq, int Nkv, int D, float scale, int causal, attn_stream_t stream) {
+  if (!mask) return ATTN_ERR_ARG;
+  if (mask_stride_b < 0 || mask_stride_h < 0 || mask_stride_q < 0) return ATTN_ERR_ARG;
+  if (mask_stride_b % 8 || mask_stride_h % 8 || mask_stride_q % 8) return ATTN_ERR_ALIGN;
+  return attn::fwd_common(q, k, v, mask, mask_stride_b, mask_stride_h, mask_stride_q, o, lse, B, Hq, Hkv, Nq, Nkv,
+                          D, scale, causal, 0, stream);
 }
 
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,

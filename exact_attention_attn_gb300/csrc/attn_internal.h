@@ -31,6 +31,11 @@ struct Problem {
   // two-tile kernel skip its copy of the second key block, so that the MMA
   // thread's bounded wait for it runs out
   int debug_flags;
+  // optional additive mask (null: none): bf16 value for (b, hq, query row i,
+  // key j) at mask[b * mask_sb + hq * mask_sh + i * mask_sq + j]; the strides
+  // are element counts, multiples of 8 (0 broadcasts that dimension)
+  const __nv_bfloat16 *mask;
+  int64_t mask_sb, mask_sh, mask_sq;
 };
 
 // Device status codes written by kernels (same values as the public ATTN_ERR_*).
@@ -59,10 +64,11 @@ struct TcConfig {
   int vring;    // V blocks travel through the Q/K ring too (Q resident, no V slot)
   int kst;      // Q/K ring depth (32 KB slots of two chunks)
   int vst;      // V-ring depth (slices)
-  uint32_t off_q, off_k, off_v, off_bar;
+  int mask_bytes;  // shared memory for one block's mask values (0 without a mask)
+  uint32_t off_q, off_k, off_v, off_m, off_bar;
   int smem_bytes;
 };
-TcConfig tc_config(int D);
+TcConfig tc_config(int D, bool mask = false);
 
 // Tensor-core kernel (tcgen05/TMEM/TMA): every D multiple of 64 up to 1024,
 // Nkv >= 1.  Bounded waits give up after wait_limit_ns.

@@ -49,6 +49,7 @@
 #include <cuda.h>
 
 #include "attn_internal.h"
+#include "attn_mask.cuh"
 #include "sm100_ptx.cuh"
 
 // Optional per-role timestamps (clock64) for 8 CTAs starting at
@@ -106,7 +107,7 @@ struct TcParams {
   int vring;     // V blocks as ring items (2 chunks each) after the next block's K
   int nvitems;   // ring items per V block when vring: ceil(vmax / 2)
   int vmax;      // chunks in the widest output slice
-  uint32_t off_q, off_k, off_v, off_bar;
+  uint32_t off_q, off_k, off_v, off_m, off_bar;
   uint64_t wait_limit_ns;
 };
 
@@ -161,6 +162,10 @@ __device__ __forceinline__ void raise_abort(Bars *bars, int *status) {
   *reinterpret_cast<volatile int *>(&bars->abort) = 1;
 }
 
+// MASK: an additive mask, staged per block and row (cp.async into shared
+// memory, issued before the row's thread waits for the block's scores) and
+// added as the scores are scaled.
+template <bool MASK>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
@@ -173,6 +178,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *sq = smem + prm.off_q;
   uint8_t *sk = smem + prm.off_k;
   uint8_t *sv = smem + prm.off_v;
+  uint8_t *smask = smem + prm.off_m;  // [16][128 rows][8 bf16] mask values of one block (MASK)
   Bars *bars = reinterpret_cast<Bars *>(smem + prm.off_bar);
   volatile int *abortf = &bars->abort;
 
@@ -410,8 +416,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float sl2 = p.scale * kLog2e;
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
+    const __nv_bfloat16 *mrow = MASK ? mask_row(p, b, hq, qi) : nullptr;
 
     for (int j = 0; j < nblk; ++j) {
+      // this row's mask values of the block travel while the scores are computed
+      if constexpr (MASK) mask_stage128(smem_u32(smask), BM, row, mrow, (jb + j) * BN, p.Nkv, p.mask);
       // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, abortf, limit))) { ok = false; break; }
       if (tid == 0) TC_TRACE_EV(12, j);
@@ -433,7 +442,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       // scale to log2 units, mask, block max
       const int kbase = (jb + j) * BN;
       float mblk = -INFINITY;
-      if (kbase + BN <= vis_end) {
+      if constexpr (MASK) {
+        // y = s * sl2 + mask * log2 e, -inf past vis_end (the thread's own
+        // copies have landed once its cp.async groups are complete)
+        cp_async_wait_all();
+        const uint4 *ms = reinterpret_cast<const uint4 *>(smask + row * 16);
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8) {
+          const uint4 w = ms[c8 * BM];
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            const int c = 8 * c8 + 2 * t4;
+            x[c] = (kbase + c < vis_end) ? fmaf(x[c], sl2, kLog2e * bf16_lo(wv[t4])) : -INFINITY;
+            x[c + 1] = (kbase + c + 1 < vis_end) ? fmaf(x[c + 1], sl2, kLog2e * bf16_hi(wv[t4])) : -INFINITY;
+            mblk = max3f(mblk, x[c], x[c + 1]);
+          }
+        }
+      } else if (kbase + BN <= vis_end) {
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           x[c] *= sl2;
@@ -568,12 +594,13 @@ constexpr int kMaxDevicesTc = 64;
 
 }  // namespace
 
-TcConfig tc_config(int D) {
+TcConfig tc_config(int D, bool mask) {
   TcConfig c;
   c.nc = D / 64;
   c.nslices = (D + 255) / 256;
   c.vmax = (c.nc + c.nslices - 1) / c.nslices;
-  const int avail = kSmemMax - kSmemReserve;
+  c.mask_bytes = mask ? BM * 256 : 0;  // one block's mask values for the 128 rows
+  const int avail = kSmemMax - kSmemReserve - c.mask_bytes;
   const int qb = c.nc * CHUNK_BYTES, vb = c.vmax * CHUNK_BYTES;
   // Q resident when it leaves room for at least three Q/K slots and one V
   // slot (two V slots if three Q/K slots still fit); else Q streams through
@@ -599,14 +626,15 @@ TcConfig tc_config(int D) {
   c.off_q = 0;
   c.off_k = c.qres ? qb : 0;
   c.off_v = c.off_k + c.kst * SLOT_BYTES;
-  c.off_bar = c.off_v + c.vst * vb;
+  c.off_m = c.off_v + c.vst * vb;
+  c.off_bar = c.off_m + c.mask_bytes;
   c.smem_bytes = c.off_bar + (int)sizeof(Bars) + 1024;  // + alignment slack
   return c;
 }
 
 cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
   static_assert(sizeof(Bars) <= kSmemReserve - 1024, "barrier block too large");
-  const TcConfig c = tc_config(p.D);
+  const TcConfig c = tc_config(p.D, p.mask != nullptr);
   if (c.kst < 2 || c.smem_bytes > kSmemMax) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
   if (!make_chunk_map(&tq, p.q, p.D, p.Nq, p.B * p.Hq, BM, c.qres ? c.nc : 2)) return cudaErrorInvalidValue;
@@ -628,20 +656,26 @@ cudaError_t launch_tc(const Problem &p, int device, uint64_t wait_limit_ns, cuda
   prm.off_q = c.off_q;
   prm.off_k = c.off_k;
   prm.off_v = c.off_v;
+  prm.off_m = c.off_m;
   prm.off_bar = c.off_bar;
   prm.wait_limit_ns = wait_limit_ns;
   const int64_t grid = (int64_t)prm.ntiles * p.B * p.Hq * c.nslices * p.kv_splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   // the opt-in shared-memory limit is a per-device function attribute: raise
-  // it to the maximum once per device
-  static std::atomic<int> attr_set[kMaxDevicesTc];
+  // it to the maximum once per device and variant
+  static std::atomic<int> attr_set[2][kMaxDevicesTc];
   if (device < 0 || device >= kMaxDevicesTc) return cudaErrorInvalidDevice;
-  if (!attr_set[device].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  const int mk = p.mask ? 1 : 0;
+  if (!attr_set[mk][device].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(mk ? attn_tc_kernel<true> : attn_tc_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
-    attr_set[device].store(1, std::memory_order_release);
+    attr_set[mk][device].store(1, std::memory_order_release);
   }
-  attn_tc_kernel<<<(unsigned)grid, THREADS, c.smem_bytes, stream>>>(tq, tk, tv, prm);
+  if (mk)
+    attn_tc_kernel<true><<<(unsigned)grid, THREADS, c.smem_bytes, stream>>>(tq, tk, tv, prm);
+  else
+    attn_tc_kernel<false><<<(unsigned)grid, THREADS, c.smem_bytes, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError();
 }
 

@@ -32,6 +32,7 @@
 #include <atomic>
 
 #include "attn_internal.h"
+#include "attn_mask.cuh"
 #include "sm100_ptx.cuh"
 
 // Optional per-role timestamps (clock64) for 8 CTAs starting at
@@ -139,13 +140,16 @@ __device__ __forceinline__ void raise_abort(Bars2 *bars, int *status) {
   *reinterpret_cast<volatile int *>(&bars->abort) = 1;
 }
 
-// POS: the scale is positive (scores and their maxima keep their order); the
-// other sign takes minima and needs no separate fast path
-template <int D, bool POS>
+// MODE 0: the scale is positive (scores and their maxima keep their order);
+// MODE 1: the scale is zero or negative (block minima of the raw scores);
+// MODE 2: an additive mask, either sign (block maxima of the masked, scaled
+// scores).  One instantiation per mode keeps each one's code small.
+template <int D, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params2 prm) {
   constexpr int NC = D / 64;  // 64-column chunks per row
+  constexpr bool POS = MODE == 0, MASK = MODE == 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -402,16 +406,50 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
     const Exp2Poly exp2_poly;
+    const __nv_bfloat16 *mrow = MASK ? mask_row(p, b, hq, qi) : nullptr;
 
     const bool tr = (tid & 127) == 0;
     // ring positions of V_j and K_{j+1}, followed by thread 0 of the tile in one
     // register: V slot bits 0-7, K slot bits 8-15, V phase bit 16, K phase bit 24
     uint32_t ring = 1u << 8;
     for (int j = 0; j < nb; ++j) {
+      const int kbase = (jb + j) * BN;
+      const bool full = kbase + BN <= vis_end;  // no masked key in this block for this row
+      // the mask values of this row and block, on their way while S_t,j is computed
+      uint32_t mk[MASK ? 64 : 1];
+      if constexpr (MASK) mask_load128(mk, mrow, kbase, p.Nkv);
       if (tr) ATTN_TRACE_EV(4 * t + 0, j);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abortf, limit))) { ok = false; break; }
       if (tr) ATTN_TRACE_EV(4 * t + 1, j);
       tc_fence_after();
+      float mblk;
+      float y[MASK ? BN : 1];
+      if constexpr (MASK) {
+        // y = s * sl2 + mask * log2 e (-inf past vis_end), kept for P; block
+        // max of y.  The scores are read a quarter at a time, so that each
+        // quarter's mask values are dead once used
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t cur[32];
+          tmem_ld32(tS + 32 * h, cur);
+          tmem_wait_ld();
+          reg_fence32(cur);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = 32 * h + 2 * i;
+            const uint32_t w = mk[16 * h + i];
+            y[c] = (kbase + c >= vis_end) ? -INFINITY : fmaf(__uint_as_float(cur[2 * i]), sl2, kLog2e * bf16_lo(w));
+            y[c + 1] =
+                (kbase + c + 1 >= vis_end) ? -INFINITY : fmaf(__uint_as_float(cur[2 * i + 1]), sl2, kLog2e * bf16_hi(w));
+            if (i & 1)
+              mx1 = max3f(mx1, y[c], y[c + 1]);
+            else
+              mx0 = max3f(mx0, y[c], y[c + 1]);
+          }
+        }
+        mblk = fmaxf(mx0, mx1);
+      } else {
       uint32_t sr[4][32];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
@@ -423,15 +461,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
-      const int kbase = (jb + j) * BN;
-      const bool full = kbase + BN <= vis_end;  // no masked key in this block for this row
       if (!full) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (kbase + c >= vis_end) x[c] = pos ? -INFINITY : INFINITY;
       }
       // block max (min when scale < 0) of the raw scores, four chains of 3-input ops
-      float mblk;
       if (pos) {
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -453,6 +488,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ext*sl2 is the block max of the scaled scores; masked-only rows give -inf
         mblk = (ext == INFINITY) ? -INFINITY : (sl2 == 0.f ? 0.f : ext * sl2);
       }
+      }  // not MASK
       const float m_new = fmaxf(m_use, mblk);
       if (__any_sync(0xffffffffu, m_new > m_use + TAU)) {
         const float alpha = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m_new);
@@ -475,7 +511,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float mu = (m_use == -INFINITY) ? 0.f : m_use;
       // the branch must be warp-uniform: both sides end in the warp-collective
       // tcgen05.st, which every lane of the warp has to execute together
-      if (pos && __all_sync(0xffffffffu, full)) {
+      if constexpr (MASK) {
+        // P = 2^(y - mu), a quarter at a time into columns [16h, 16h+16)
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = 32 * h + 2 * i;
+            const float p0 = ex2_approx(y[c] - mu), p1 = ex2_approx(y[c + 1] - mu);
+            ls[i & 3] += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + h * 16, pk);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      } else if (pos && __all_sync(0xffffffffu, full)) {
         // every key visible and scale > 0: y = s*sl2 - mu on f32x2 pairs,
         // exp2 on the MUFU (pairs selected by kPolyPairs on the FMA pipe)
         // The scores are read again from TMEM a quarter at a time (the next
@@ -651,7 +703,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int D, bool POS>
+template <int D, int MODE>
 cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
   constexpr int NC = D / 64;
   const int avail = kSmemMax - 2048;
@@ -690,13 +742,13 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
   static std::atomic<int> attr_set[64];
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[device].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc2_kernel<D, POS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc2_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
     attr_set[device].store(1, std::memory_order_release);
   }
   const int64_t grid = (int64_t)prm.npairs * p.B * p.Hq * p.kv_splits;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  attn_tc2_kernel<D, POS><<<(unsigned)grid, THREADS, smem, stream>>>(tq, tk, tv, prm);
+  attn_tc2_kernel<D, MODE><<<(unsigned)grid, THREADS, smem, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError();
 }
 
@@ -707,10 +759,15 @@ bool tc2_supports(int D) { return D == 64 || D == 128; }
 cudaError_t launch_tc2(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
   // the same product as the kernel's, so that both sides agree on its sign
   const bool pos = p.scale * kLog2e > 0.f;
-  if (p.D == 64) return pos ? launch_tc2_d<64, true>(p, device, wait_limit_ns, stream)
-                            : launch_tc2_d<64, false>(p, device, wait_limit_ns, stream);
-  if (p.D == 128) return pos ? launch_tc2_d<128, true>(p, device, wait_limit_ns, stream)
-                             : launch_tc2_d<128, false>(p, device, wait_limit_ns, stream);
+  if (p.D == 64) {
+    if (p.mask) return launch_tc2_d<64, 2>(p, device, wait_limit_ns, stream);
+    return pos ? launch_tc2_d<64, 0>(p, device, wait_limit_ns, stream) : launch_tc2_d<64, 1>(p, device, wait_limit_ns, stream);
+  }
+  if (p.D == 128) {
+    if (p.mask) return launch_tc2_d<128, 2>(p, device, wait_limit_ns, stream);
+    return pos ? launch_tc2_d<128, 0>(p, device, wait_limit_ns, stream)
+               : launch_tc2_d<128, 1>(p, device, wait_limit_ns, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

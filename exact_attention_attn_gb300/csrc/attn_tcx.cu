@@ -55,6 +55,7 @@
 #include <cuda.h>
 
 #include "attn_internal.h"
+#include "attn_mask.cuh"
 #include "sm100_ptx.cuh"
 
 // Optional per-role timestamps (clock64) of the first cluster, compiled in only
@@ -94,7 +95,7 @@ struct XParams {
   Problem p;
   int ntiles;
   int kst;
-  uint32_t off_k, off_x, off_p, off_a, off_s, off_sa, off_bar;
+  uint32_t off_k, off_x, off_p, off_a, off_s, off_sa, off_m, off_bar;
   uint64_t wait_limit_ns;
 };
 
@@ -165,8 +166,10 @@ __device__ __forceinline__ void raise_abort_cluster(XBars *bars, int *status, ui
 // NX CTAs per cluster, each with a slice of SC 64-column chunks (D = 64 NX SC),
 // K and V travelling through the ring as items of IC chunks -- or, UN, slices
 // of SC or SC - 1 chunks (D = 64 nc with nc not a multiple of NX) whose K and
-// V travel as one-chunk items.
-template <int NX, int SC, bool UN>
+// V travel as one-chunk items.  MASK: an additive mask, staged per block for
+// the owner rows (cp.async into shared memory, issued before the owner
+// waits for the block's scores) and added as the scores are scaled.
+template <int NX, int SC, bool UN, bool MASK>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tcx_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ XParams prm) {
@@ -185,6 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *sp = smem + prm.off_p;
   float *salpha = reinterpret_cast<float *>(smem + prm.off_a);  // [128], by tile row
   uint8_t *sst = smem + prm.off_s;                               // staged own P rows
+  uint8_t *smask = smem + prm.off_m;                             // owner rows' mask values (MASK)
   float *sstal = reinterpret_cast<float *>(smem + prm.off_sa);    // staged own rescale factors
   // l[128], m[128] of every row at the end, in the Q region: every CTA's last
   // Q K^T has completed before any owner sends them (it needed their partials)
@@ -469,7 +473,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       return true;
     };
 
+    const __nv_bfloat16 *mrow = MASK ? mask_row(p, b, hq, qi) : nullptr;
     for (int j = 0; j < nblk && ok; ++j) {
+      // an owner's mask values of this block travel while it waits for the scores
+      if (MASK && is_owner) mask_stage128(smem_u32(smask), R, orow, mrow, (jb + j) * BN, p.Nkv, p.mask);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, abortf, limit))) { ok = false; break; }
       tc_fence_after();
       const uint32_t pcol = (j & 1) ? TM_P1 : TM_P0;
@@ -560,7 +567,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // scale to log2 units, mask, block max
       const int kbase = (jb + j) * BN;
-      if (kbase + BN <= vis_end) {
+      if constexpr (MASK) {
+        // y = s * sl2 + mask * log2 e, -inf past vis_end; this thread's own
+        // copies have landed once its cp.async groups are complete
+        cp_async_wait_all();
+        const uint4 *ms = reinterpret_cast<const uint4 *>(smask + orow * 16);
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8) {
+          const uint4 w = ms[c8 * R];
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int c = 8 * c8 + 2 * t;
+            x[c] = (kbase + c < vis_end) ? fmaf(x[c], sl2, kLog2e * bf16_lo(wv[t])) : -INFINITY;
+            x[c + 1] = (kbase + c + 1 < vis_end) ? fmaf(x[c + 1], sl2, kLog2e * bf16_hi(wv[t])) : -INFINITY;
+          }
+        }
+      } else if (kbase + BN <= vis_end) {
 #pragma unroll
         for (int c = 0; c < BN; ++c) x[c] *= sl2;
       } else {
@@ -730,7 +753,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int NX, int SC, bool UN>
+template <int NX, int SC, bool UN, bool MASK>
 struct XLayout {
   static constexpr int R = BM / NX;
   static constexpr int QB = SC * CHUNK_BYTES;
@@ -741,15 +764,16 @@ struct XLayout {
   static constexpr int AB = BM * 4;
   static constexpr int SB = R * 256;
   static constexpr int SAB = 512;
+  static constexpr int MB = MASK ? R * 256 : 0;  // owner rows' mask values of one block
 };
 
-template <int NX, int SC, bool UN>
+template <int NX, int SC, bool UN, bool MASK>
 cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
-  using L = XLayout<NX, SC, UN>;
+  using L = XLayout<NX, SC, UN, MASK>;
   constexpr int ITEM_BYTES = L::ITEM_BYTES;
   static_assert(sizeof(XBars) <= 1024, "barrier block too large");
   constexpr int kBarBytes = (int)((sizeof(XBars) + 127) / 128 * 128);
-  const int fixed = L::QB + L::XB + L::PB + L::AB + L::SB + L::SAB + kBarBytes + 1024 /* alignment */;
+  const int fixed = L::QB + L::XB + L::PB + L::AB + L::SB + L::SAB + L::MB + kBarBytes + 1024 /* alignment */;
   int kst = (kSmemMax - fixed) / ITEM_BYTES;
   if (kst > MAX_KST) kst = MAX_KST;
   if (kst < 2) return cudaErrorInvalidConfiguration;
@@ -764,7 +788,8 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   prm.off_a = prm.off_p + L::PB;
   prm.off_s = prm.off_a + L::AB;
   prm.off_sa = prm.off_s + L::SB;
-  prm.off_bar = prm.off_sa + L::SAB;
+  prm.off_m = prm.off_sa + L::SAB;
+  prm.off_bar = prm.off_m + L::MB;
   prm.wait_limit_ns = wait_limit_ns;
   const int smem = (int)prm.off_bar + kBarBytes + 1024;
   if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
@@ -775,7 +800,7 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   static std::atomic<int> attr_set[64];
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[device].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tcx_kernel<NX, SC, UN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    cudaError_t e = cudaFuncSetAttribute(attn_tcx_kernel<NX, SC, UN, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
     attr_set[device].store(1, std::memory_order_release);
   }
@@ -800,7 +825,7 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
   int f = fits[device].load(std::memory_order_relaxed);
   if (f == 0) {
     int nclusters = 0;
-    cudaError_t q = cudaOccupancyMaxActiveClusters(&nclusters, attn_tcx_kernel<NX, SC, UN>, &cfg);
+    cudaError_t q = cudaOccupancyMaxActiveClusters(&nclusters, attn_tcx_kernel<NX, SC, UN, MASK>, &cfg);
     if (q != cudaSuccess) {
       cudaGetLastError();
       nclusters = 0;
@@ -809,7 +834,7 @@ cudaError_t launch_tcx_n(const Problem &p, int device, uint64_t wait_limit_ns, c
     fits[device].store(f, std::memory_order_relaxed);
   }
   if (f != 1) return cudaErrorNotSupported;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tcx_kernel<NX, SC, UN>, tq, tk, tv, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tcx_kernel<NX, SC, UN, MASK>, tq, tk, tv, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -832,17 +857,23 @@ bool tcx_supports(int D) {
 #endif
 }
 
-cudaError_t launch_tcx(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
-  if (p.D == 384) return launch_tcx_n<2, 3, false>(p, device, wait_limit_ns, stream);
-  if (p.D == 512) return launch_tcx_n<2, 4, false>(p, device, wait_limit_ns, stream);
-  if (p.D == 768) return launch_tcx_n<4, 3, false>(p, device, wait_limit_ns, stream);
-  if (p.D == 1024) return launch_tcx_n<4, 4, false>(p, device, wait_limit_ns, stream);
+template <bool MASK>
+cudaError_t launch_tcx_m(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
+  if (p.D == 384) return launch_tcx_n<2, 3, false, MASK>(p, device, wait_limit_ns, stream);
+  if (p.D == 512) return launch_tcx_n<2, 4, false, MASK>(p, device, wait_limit_ns, stream);
+  if (p.D == 768) return launch_tcx_n<4, 3, false, MASK>(p, device, wait_limit_ns, stream);
+  if (p.D == 1024) return launch_tcx_n<4, 4, false, MASK>(p, device, wait_limit_ns, stream);
   // uneven slices: 2 CTAs up to D = 512, 4 above, at most four chunks each
   const int nc = p.D / 64;
-  if (nc == 7) return launch_tcx_n<2, 4, true>(p, device, wait_limit_ns, stream);
-  if (nc >= 9 && nc <= 11) return launch_tcx_n<4, 3, true>(p, device, wait_limit_ns, stream);
-  if (nc >= 13 && nc <= 15) return launch_tcx_n<4, 4, true>(p, device, wait_limit_ns, stream);
+  if (nc == 7) return launch_tcx_n<2, 4, true, MASK>(p, device, wait_limit_ns, stream);
+  if (nc >= 9 && nc <= 11) return launch_tcx_n<4, 3, true, MASK>(p, device, wait_limit_ns, stream);
+  if (nc >= 13 && nc <= 15) return launch_tcx_n<4, 4, true, MASK>(p, device, wait_limit_ns, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tcx(const Problem &p, int device, uint64_t wait_limit_ns, cudaStream_t stream) {
+  return p.mask ? launch_tcx_m<true>(p, device, wait_limit_ns, stream)
+                : launch_tcx_m<false>(p, device, wait_limit_ns, stream);
 }
 
 }  // namespace attn

@@ -167,6 +167,16 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int x, i
                : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, L2 only); the first
+// src_bytes (0..16) bytes are read, the rest of the 16 are zero-filled.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until every cp.async group this thread committed has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -82,9 +82,8 @@ typedef struct CUstream_st *attn_stream_t;
  * reaches the work.  o must not overlap q, k, v or lse.  Every base address
  * must be 16-byte aligned.  The call validates its arguments on the host,
  * launches asynchronously on `stream` and returns without waiting.  It may
- * allocate a stream-ordered split-KV workspace (cudaMallocAsync on `stream`,
- * freed on the same stream after use) when the problem has too few query
- * tiles to fill the GPU.  Bounded device-side waits that run out are not
+ * take a stream-ordered split-KV workspace (see attn_fwd_splitkv) when the
+ * problem has too few query tiles to fill the GPU.  Bounded device-side waits that run out are not
  * reported here: call attn_fwd_status.
  *
  * CUDA graphs: the call keeps no state between calls that a graph replay
@@ -113,14 +112,51 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, floa
  *
  * kv_splits: 0 chooses automatically (what attn_fwd does); 1 disables the
  *   split; 2..64 forces that many ranges (ranges left empty are harmless).
- * Workspace: kv_splits * B * Hq * Nq * (D + 1) * 4 bytes, taken with
- *   cudaMallocAsync on `stream` and released with cudaFreeAsync on the same
- *   stream after the merge; ATTN_ERR_NOMEM if it cannot be had.
+ * Workspace: kv_splits * B * Hq * Nq * (D + 1) * 4 bytes, stream-ordered on
+ *   `stream` (allocated before the kernels, freed after the merge) from a
+ *   memory pool of the library's that keeps its memory between calls (a
+ *   device holds up to the largest workspace asked for, until the process
+ *   exits); while `stream` is being captured into a CUDA graph it is taken
+ *   with cudaMallocAsync instead (a graph memory node).  ATTN_ERR_NOMEM if it
+ *   cannot be had.
  * Everything else (arguments, layouts, asynchrony, errors) is as attn_fwd.
  */
 ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
                               int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                               float scale, int causal, int kv_splits, attn_stream_t stream);
+
+/*
+ * attn_fwd_masked -- attn_fwd with an additive attention mask.
+ *
+ * The FFPA README's feature table lists a mask besides the causal one
+ * ("Causal/Mask"); it is read here as SDPA's additive float mask.  With
+ * M[b, hq, i, j] the mask value, the scores become
+ *
+ *     S_ij = scale * Q[b,hq]_i . K[b,kv]_j + M[b, hq, i, j]
+ *
+ * before the row softmax; an entry of -inf hides key j from query i, and the
+ * causal flag, if set, hides j > i + (Nkv - Nq) on top.  LSE is ln sum_j
+ * exp(S_ij) over the visible keys; a row whose keys are all hidden gets
+ * O = 0 and LSE = -inf.
+ *
+ * mask   device pointer, bf16; the value for (b, hq, i, j) is at element
+ *        b * mask_stride_b + hq * mask_stride_h + i * mask_stride_q + j.
+ *        Keys (j) are contiguous.  Strides are element counts >= 0 and
+ *        multiples of 8 (16 bytes); a stride of 0 broadcasts that dimension
+ *        (e.g. one [Nq, Nkv] mask for every batch and head, or a key-padding
+ *        mask [B, 1, 1, Nkv] with mask_stride_h = mask_stride_q = 0).  The
+ *        base must be 16-byte aligned.  Values must be finite or -inf
+ *        (+inf and NaN give undefined results).  Every element the strides
+ *        address for j < Nkv must be readable; nothing past Nkv is read.
+ * Everything else (arguments, layouts, automatic key splits, asynchrony,
+ * errors, CUDA-graph capture) is as attn_fwd.  Returns ATTN_ERR_ARG for a
+ * null mask or a negative stride, ATTN_ERR_ALIGN for a stride that is not a
+ * multiple of 8 or a misaligned base.
+ */
+ATTN_API int attn_fwd_masked(const void *q, const void *k, const void *v, const void *mask,
+                             long long mask_stride_b, long long mask_stride_h, long long mask_stride_q,
+                             void *o, float *lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                             float scale, int causal, attn_stream_t stream);
 
 /*
  * attn_fwd_host -- attn_fwd on host buffers.

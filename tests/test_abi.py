@@ -147,3 +147,25 @@ def test_plain_c_client(lib, tmp_path):
     args = [] if torch.cuda.is_available() else ["--no-device"]
     r = subprocess.run([exe] + args, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and "OK" in r.stdout, r.stdout + r.stderr
+
+
+def test_masked_entry_argument_errors(lib):
+    import ctypes as C
+    lib.attn_fwd_masked.argtypes = ([C.c_void_p] * 4 + [C.c_longlong] * 3 + [C.c_void_p] * 2 + [C.c_int] * 6 +
+                                    [C.c_float, C.c_int, C.c_void_p])
+    b = Buf()
+    p = b.p
+    ARG, ALIGN = -1, -2
+
+    def masked(mask, sb=0, sh=0, sq=8, D=64, causal=0, B=1):
+        return lib.attn_fwd_masked(p, p, p, mask, sb, sh, sq, p, p, B, 2, 1, 8, 8, D, 0.125, causal, None)
+
+    assert masked(None) == ARG                 # a mask is required
+    assert masked(p, sq=-8) == ARG             # negative stride
+    assert masked(p, sb=-16) == ARG
+    assert masked(p, sq=12) == ALIGN           # not a multiple of 8 elements
+    assert masked(p, sh=4) == ALIGN
+    assert masked(p + 2) == ALIGN              # misaligned base
+    assert masked(p, D=96) == ARG              # the size checks of attn_fwd
+    assert masked(p, causal=3) == ARG
+    assert masked(p, B=0) == 0                 # empty problem: nothing to do
