@@ -64,6 +64,8 @@ def load_library() -> ctypes.CDLL:
         ll = ctypes.c_longlong
         lib.attn_fwd_masked.argtypes = [vp, vp, vp, vp, ll, ll, ll, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd_masked.restype = ci
+        lib.attn_bwd.argtypes = [vp] * 9 + [ci] * 6 + [cf, ci, vp]
+        lib.attn_bwd.restype = ci
         lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd_host.restype = ci
         lib.attn_set_debug.argtypes = [ci, ctypes.c_longlong]
@@ -179,6 +181,42 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | N
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return out, lse
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+             dout: torch.Tensor, scale: float | None = None, causal: bool = False, stream=None,
+             dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None):
+    """dq, dk, dv = gradients of attention forward (attn_bwd of the C ABI).
+
+    q, k, v, o, dout bf16 and lse fp32 as attn_fwd takes and returns them;
+    head dim 64 or 128.  Runs asynchronously on ``stream``.
+    """
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(lse, "lse", torch.float32, 3)
+    B, Hq, Nq, D = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError(f"k {tuple(k.shape)} / v {tuple(v.shape)} do not match q {tuple(q.shape)}")
+    if o.shape != q.shape or dout.shape != q.shape or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("o / dout / lse shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n, ref in ((dq, "dq", q), (dk, "dk", k), (dv, "dv", v)):
+        _check(t, n, torch.bfloat16, 4)
+        if t.shape != ref.shape:
+            raise ValueError(f"{n} shape mismatch")
+    with torch.cuda.device(q.device):
+        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Nq, Nkv, D, float(scale),
+                          int(bool(causal)), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def _check_host(t: torch.Tensor, name: str, dtype, ndim: int) -> None:

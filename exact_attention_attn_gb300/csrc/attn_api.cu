@@ -235,6 +235,12 @@ int current_device(int *device, int *sm_count, int **status) {
 
 int record_cuda_error(cudaError_t e) { return record(e); }
 
+cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t st) {
+  DeviceInfo *d = nullptr;
+  if (device_info(&d) != ATTN_OK) return cudaErrorInvalidDevice;
+  return workspace_alloc(*d, ptr, bytes, st);
+}
+
 // The tensor-core kernel for the head dim: two-tile (D 64, 128), cluster
 // Split-D (D 384 ... 1024), else the Split-D kernel with per-slice scores.
 cudaError_t launch_tensor(const Problem &p, int device, cudaStream_t st) {

@@ -90,6 +90,11 @@ cudaError_t launch_tc2(const Problem &p, int device, uint64_t wait_limit_ns, cud
 // exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.  Memory-bound, one pass.
 cudaError_t launch_combine(const Problem &p, cudaStream_t stream);
 
+// Stream-ordered scratch from the current device's library pool (the one the
+// split-KV workspace comes from; cudaMallocAsync while `st` is captured).
+// Free with cudaFreeAsync on the same stream.
+cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t st);
+
 // Bound on device-side waits and debug flags currently set by attn_set_debug.
 uint64_t wait_limit_ns();
 int debug_flags();

@@ -130,6 +130,15 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *m
       : "memory");
 }
 
+// Plain (untiled) bulk copy global -> shared of `bytes` bytes (a multiple of
+// 16; both addresses 16-byte aligned), completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // 4-D tiled bulk tensor copy shared -> global (coordinates innermost first);
 // elements outside the tensor are not written.  Completion is tracked by the
 // issuing thread's bulk async-group.

@@ -237,6 +237,39 @@ ATTN_API int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *
                                       float scale, int causal, int kv_splits, attn_stream_t stream);
 
 /*
+ * attn_bwd -- exact attention backward: the gradients of attn_fwd's O with
+ * respect to q, k and v, given the upstream gradient dout of O.
+ *
+ * With P the row softmax of S = scale * Q K^T (causal entries hidden as in
+ * attn_fwd; P = 0 where hidden) and O = P V, the chain rule through the row
+ * softmax gives
+ *     dV = P^T dO,   dP = dO V^T,   Delta_i = sum_d dO_id O_id,
+ *     dS = P * (dP - Delta),   dQ = scale * dS K,   dK = scale * dS^T Q,
+ * and a key/value head shared by a GQA group receives the sum over its query
+ * heads.  As the FlashAttention pages describe the backward pass ("FlashAttention
+ * v1/v2/v3/v4", "FA1 -- el cambio de orden de las operaciones"; the
+ * FlashAttention summary card), S is recomputed block by block from Q, K and
+ * the forward's row statistics (here LSE); nothing N x N is stored.
+ *
+ * q, k, v   the forward's inputs (layouts of attn_fwd).
+ * o, lse    the forward's outputs for these inputs (attn_fwd's O and LSE).
+ * dout      bf16 [B, Hq, Nq, D], the gradient of the loss with respect to O.
+ * dq        bf16 [B, Hq, Nq, D]; dk, dv bf16 [B, Hkv, Nkv, D]: fully written.
+ * D         64 or 128 (other head dims: ATTN_ERR_ARG).
+ * Every other argument, the checks, alignment (16 bytes for every pointer)
+ * and asynchrony are as attn_fwd.  Rows that see no key get dq = 0; keys
+ * that no query sees get dk = dv = 0.  The result is deterministic (no
+ * atomics: one kernel accumulates dK, dV per key tile over the queries of
+ * the whole GQA group, another dQ per query tile over the keys).  A
+ * stream-ordered scratch of 2 * B * Hq * ceil(Nq / 128) * 128 * 4 bytes is
+ * taken from the library's pool (see attn_fwd_splitkv); ATTN_ERR_NOMEM if it
+ * cannot be had.  The additive mask of attn_fwd_masked has no backward here.
+ */
+ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                      const float *lse, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Nq, int Nkv,
+                      int D, float scale, int causal, attn_stream_t stream);
+
+/*
  * attn_fwd_status -- synchronise `stream`, then read and clear the device
  * status word of the current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a
  * bounded mbarrier wait inside a kernel gave up; that kernel's outputs are

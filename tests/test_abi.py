@@ -169,3 +169,25 @@ def test_masked_entry_argument_errors(lib):
     assert masked(p, D=96) == ARG              # the size checks of attn_fwd
     assert masked(p, causal=3) == ARG
     assert masked(p, B=0) == 0                 # empty problem: nothing to do
+
+
+def test_backward_entry_argument_errors(lib):
+    import ctypes as C
+    lib.attn_bwd.argtypes = [C.c_void_p] * 9 + [C.c_int] * 6 + [C.c_float, C.c_int, C.c_void_p]
+    b = Buf()
+    p = b.p
+    ARG, ALIGN = -1, -2
+
+    def bwd(D=64, ptrs=None, causal=0, B=1, Nq=8, Nkv=8, scale=0.125):
+        ptrs = ptrs or [p] * 9
+        return lib.attn_bwd(*ptrs, B, 2, 1, Nq, Nkv, D, scale, causal, None)
+
+    assert bwd(D=256) == ARG                   # head dims 64 and 128 only
+    assert bwd(D=96) == ARG
+    assert bwd(causal=2) == ARG
+    assert bwd(scale=float("nan")) == ARG
+    assert bwd(ptrs=[p] * 5 + [None] + [p] * 3) == ARG   # no lse
+    assert bwd(ptrs=[p] * 8 + [None]) == ARG              # no dv
+    assert bwd(ptrs=[p + 4] + [p] * 8) == ALIGN
+    assert bwd(ptrs=[p] * 6 + [p + 8] + [p] * 2) == ALIGN
+    assert bwd(B=0, ptrs=[None] * 9) == 0                # empty problem
