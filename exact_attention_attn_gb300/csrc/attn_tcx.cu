@@ -201,15 +201,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint64_t limit = prm.wait_limit_ns;
   const uint32_t me = cluster_ctarank();
 
-  // ---- work unit (one per cluster): (b, hq) fastest, then query tile
-  //      (heaviest causal tiles first); the CTA's rank is its D slice
+  // ---- work unit (one per cluster): query tile fastest, then (b, hq); the
+  //      CTA's rank is its D slice
   int cid = (int)(blockIdx.x / NX);
   const int nsplit = p.kv_splits;
   const int split = cid % nsplit;
   cid /= nsplit;
   const int BH = p.B * p.Hq;
-  const int bh = cid % BH;
-  const int tt = cid / BH;
+  // the tiles of one head one after the other (heaviest causal tiles first),
+  // so that a wave of clusters streams the K/V of few heads and each block
+  // comes from L2 to every tile of its head: on B1 H8 N4096 D512 the DRAM
+  // reads fall from 2.1x to 1.0x the algorithmic bytes (head-fastest order)
+  const int bh = cid / prm.ntiles;
+  const int tt = cid % prm.ntiles;
   const int tile = p.causal ? (prm.ntiles - 1 - tt) : tt;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
