@@ -7,3 +7,4 @@ from .attention import (attention, attention_backward, attention_backward_head, 
                         attention_bruteforce, attention_head,
                         attention_online_head, causal_visible, kv_head_of, lse_merge,
                         probs_head, scores_head)
+from . import fp8  # noqa: F401,E402
