@@ -6,8 +6,8 @@ of ``include/attn.h``); this package only marshals torch tensors into that
 call.  Importing the package does not load the library; the first call does,
 and raises if the library has not been built.
 """
-from .binding import (AttnError, attn_bwd, attn_fwd, attn_fwd_host, attn_fwd_plan, attn_fwd_status, attn_set_debug, attn_strerror,  # noqa: F401
+from .binding import (AttnError, attn_bwd, attn_fp8_quantize, attn_fwd, attn_fwd_fp8, attn_fwd_host, attn_fwd_plan, attn_fwd_status, attn_set_debug, attn_strerror,  # noqa: F401
                       attn_version, library_path, load_library)
 
-__all__ = ["AttnError", "attn_bwd", "attn_fwd", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_status", "attn_set_debug", "attn_strerror", "attn_version",
+__all__ = ["AttnError", "attn_bwd", "attn_fp8_quantize", "attn_fwd", "attn_fwd_fp8", "attn_fwd_host", "attn_fwd_plan", "attn_fwd_status", "attn_set_debug", "attn_strerror", "attn_version",
            "library_path", "load_library"]

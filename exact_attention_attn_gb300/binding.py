@@ -64,6 +64,10 @@ def load_library() -> ctypes.CDLL:
         ll = ctypes.c_longlong
         lib.attn_fwd_masked.argtypes = [vp, vp, vp, vp, ll, ll, ll, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
         lib.attn_fwd_masked.restype = ci
+        lib.attn_fp8_quantize.argtypes = [vp] * 9 + [ci] * 6 + [vp]
+        lib.attn_fp8_quantize.restype = ci
+        lib.attn_fwd_fp8.argtypes = [vp] * 8 + [ci] * 6 + [cf, ci, vp]
+        lib.attn_fwd_fp8.restype = ci
         lib.attn_bwd.argtypes = [vp] * 9 + [ci] * 6 + [cf, ci, vp]
         lib.attn_bwd.restype = ci
         lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
@@ -217,6 +221,60 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_fp8_quantize(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> dict:
+    """FP8 operands of bf16 q, k, v (head dim 128): attn_fp8_quantize of the
+    C ABI.  Returns a dict of q8, k8, vt8 (uint8) and sq, sk, sv (fp32)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, 4)
+    B, Hq, Nq, D = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError(f"k {tuple(k.shape)} / v {tuple(v.shape)} do not match q {tuple(q.shape)}")
+    dev = q.device
+    nkb = (Nkv + 127) // 128
+    out = {
+        "q8": torch.empty((B, Hq, Nq, D), dtype=torch.uint8, device=dev),
+        "k8": torch.empty((B, Hkv, Nkv, D), dtype=torch.uint8, device=dev),
+        "vt8": torch.empty((B, Hkv, D, nkb * 128), dtype=torch.uint8, device=dev),
+        "sq": torch.empty((B, Hq, (Nq + 127) // 128), dtype=torch.float32, device=dev),
+        "sk": torch.empty((B, Hkv, nkb), dtype=torch.float32, device=dev),
+        "sv": torch.empty((B, Hkv), dtype=torch.float32, device=dev),
+    }
+    with torch.cuda.device(dev):
+        rc = lib.attn_fp8_quantize(q.data_ptr(), k.data_ptr(), v.data_ptr(), out["q8"].data_ptr(),
+                                   out["k8"].data_ptr(), out["vt8"].data_ptr(), out["sq"].data_ptr(),
+                                   out["sk"].data_ptr(), out["sv"].data_ptr(), B, Hq, Hkv, Nq, Nkv, D,
+                                   _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fp8_quantize")
+    return out
+
+
+def attn_fwd_fp8(qz: dict, scale: float | None = None, causal: bool = False, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, stream=None):
+    """O, LSE of the FP8 path from attn_fp8_quantize's operands."""
+    lib = load_library()
+    B, Hq, Nq, D = qz["q8"].shape
+    Hkv, Nkv = qz["k8"].shape[1], qz["k8"].shape[2]
+    dev = qz["q8"].device
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, Nq, D), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    _check(out, "out", torch.bfloat16, 4)
+    _check(lse, "lse", torch.float32, 3)
+    with torch.cuda.device(dev):
+        rc = lib.attn_fwd_fp8(qz["q8"].data_ptr(), qz["k8"].data_ptr(), qz["vt8"].data_ptr(), qz["sq"].data_ptr(),
+                              qz["sk"].data_ptr(), qz["sv"].data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+                              Nq, Nkv, D, float(scale), int(bool(causal)), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8")
+    return out, lse
 
 
 def _check_host(t: torch.Tensor, name: str, dtype, ndim: int) -> None:

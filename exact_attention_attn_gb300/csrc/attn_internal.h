@@ -55,6 +55,10 @@ bool make_block_map(CUtensorMap *m, const void *base, int cols, int rows, int pl
 // to the copy (chunks past the last one read as zeros).
 bool make_chunk_map(CUtensorMap *m, const void *base, int cols, int rows, int planes, int box_rows, int box_chunks);
 
+// TMA map of a [planes, rows, inner] byte tensor (inner contiguous, at least
+// 128 and a multiple of 16) with 128 x 128-byte boxes and the 128-byte swizzle.
+bool make_u8_map(CUtensorMap *m, const void *base, int inner, int rows, int planes);
+
 // Shared-memory plan of the tensor-core kernel for head dim D.
 struct TcConfig {
   int nc;       // 64-column chunks of D

@@ -270,6 +270,43 @@ ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o
                       int D, float scale, int causal, attn_stream_t stream);
 
 /*
+ * attn_fp8_quantize / attn_fwd_fp8 -- FP8 (e4m3) attention forward, head
+ * dim 128.
+ *
+ * The FP8 scheme of the FlashAttention blog ("FlashAttention v1/v2/v3/v4",
+ * "FA3 -- el momento Hopper": per-tile scales and a Hadamard-based rotation
+ * before quantising) and of the ZYFA page (a Hadamard rotation of Q and K,
+ * power-of-two descales, probabilities scaled by a power of two before they
+ * are rounded to FP8).  attn_fp8_quantize turns bf16 q, k, v into:
+ *   q8   uint8 [B, Hq, Nq, 128]: e4m3 codes of (q_row H / sqrt(128)) / sq,
+ *        H the Sylvester Hadamard matrix, per 128-row block of one head;
+ *   sq   float [B, Hq, ceil(Nq/128)]: the blocks' scales, powers of two, the
+ *        smallest 2^k with max |x| <= 448 * 2^k;
+ *   k8, sk  the same for k: [B, Hkv, Nkv, 128] and [B, Hkv, ceil(Nkv/128)];
+ *   vt8  uint8 [B, Hkv, 128, nkv_pad], nkv_pad = 128 * ceil(Nkv / 128): e4m3
+ *        codes of v / sv, transposed (keys contiguous), code 0 past Nkv;
+ *   sv   float [B, Hkv]: one power-of-two scale per (b, kv head).
+ * attn_fwd_fp8 computes O (bf16 [B, Hq, Nq, 128]) and LSE (fp32 [B, Hq, Nq])
+ * from them: S = sq sk (q8 k8^T) on the FP8 tensor cores (the rotation
+ * cancels: (qH)(kH)^T = q k^T), the online softmax of attn_fwd with a lazy
+ * rescale threshold of 0.5 (log2 units), P rounded to e4m3 as 2^8 p, and
+ * O = sv (P8 v8) / (2^8 l) with l the fp32 sum of p.  The result approximates
+ * attn_fwd's; it equals exact attention on the dequantised inputs up to the
+ * e4m3 rounding of P.
+ *
+ * D must be 128; attn_fwd_fp8 also needs a finite scale > 0 (ATTN_ERR_ARG
+ * otherwise).  Every pointer is a device pointer owned by the caller, 16-byte
+ * aligned; sizes, causal masking (bottom-right), rows with no key, GQA,
+ * asynchrony and errors are as attn_fwd.  No key-range splits.
+ */
+ATTN_API int attn_fp8_quantize(const void *q, const void *k, const void *v, void *q8, void *k8, void *vt8,
+                               float *sq, float *sk, float *sv, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                               attn_stream_t stream);
+ATTN_API int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *sq, const float *sk,
+                          const float *sv, void *o, float *lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                          float scale, int causal, attn_stream_t stream);
+
+/*
  * attn_fwd_status -- synchronise `stream`, then read and clear the device
  * status word of the current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a
  * bounded mbarrier wait inside a kernel gave up; that kernel's outputs are

@@ -191,3 +191,20 @@ def test_backward_entry_argument_errors(lib):
     assert bwd(ptrs=[p + 4] + [p] * 8) == ALIGN
     assert bwd(ptrs=[p] * 6 + [p + 8] + [p] * 2) == ALIGN
     assert bwd(B=0, ptrs=[None] * 9) == 0                # empty problem
+
+
+def test_fp8_entry_argument_errors(lib):
+    import ctypes as C
+    lib.attn_fp8_quantize.argtypes = [C.c_void_p] * 9 + [C.c_int] * 6 + [C.c_void_p]
+    lib.attn_fwd_fp8.argtypes = [C.c_void_p] * 8 + [C.c_int] * 6 + [C.c_float, C.c_int, C.c_void_p]
+    b = Buf()
+    p = b.p
+    ARG, ALIGN = -1, -2
+    assert lib.attn_fp8_quantize(*([p] * 9), 1, 2, 1, 8, 8, 64, None) == ARG    # head dim 128 only
+    assert lib.attn_fp8_quantize(*([p] * 8), None, 1, 2, 1, 8, 8, 128, None) == ARG
+    assert lib.attn_fp8_quantize(p + 4, *([p] * 8), 1, 2, 1, 8, 8, 128, None) == ALIGN
+    assert lib.attn_fwd_fp8(*([p] * 8), 1, 2, 1, 8, 8, 128, 0.0, 0, None) == ARG   # scale must be > 0
+    assert lib.attn_fwd_fp8(*([p] * 8), 1, 2, 1, 8, 8, 128, float("nan"), 0, None) == ARG
+    assert lib.attn_fwd_fp8(*([p] * 8), 1, 2, 1, 8, 8, 128, 0.1, 2, None) == ARG
+    assert lib.attn_fwd_fp8(*([p] * 8), 1, 2, 1, 8, 8, 256, 0.1, 0, None) == ARG
+    assert lib.attn_fwd_fp8(*([None] * 8), 0, 2, 1, 8, 8, 128, 0.1, 0, None) == 0
