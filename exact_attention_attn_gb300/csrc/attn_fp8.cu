@@ -61,15 +61,25 @@ constexpr int kSmemMax = 232448;
 
 // ---------------------------------------------------------------- quantisation
 
-// 2^k for the smallest integer k with amax <= 448 2^k; 1 when amax == 0.
+// k for the smallest integer k with amax <= 448 2^k; 0 when amax == 0.
 // With amax = m 2^e, m in [0.5, 1), and 448 = 0.875 2^9: k = e - 9, plus one
 // when m > 0.875.
-__device__ __forceinline__ float pow2_scale(float amax) {
-  if (!(amax > 0.f)) return 1.f;
+__device__ __forceinline__ int pow2_exp(float amax) {
+  if (!(amax > 0.f)) return 0;
   int e;
   const float m = frexpf(amax, &e);
-  return ldexpf(1.f, e - 9 + (m > 0.875f ? 1 : 0));
+  return e - 9 + (m > 0.875f ? 1 : 0);
 }
+__device__ __forceinline__ float pow2_scale(float amax) { return ldexpf(1.f, pow2_exp(amax)); }
+
+// x / 2^k exactly: a multiply by 2^-k where that is a normal float, else a
+// division (inputs that small do not occur in practice).
+struct InvPow2 {
+  float s, inv;
+  bool mul;
+  __device__ __forceinline__ explicit InvPow2(int k) : s(ldexpf(1.f, k)), inv(ldexpf(1.f, -k)), mul(k > -126 && k < 126) {}
+  __device__ __forceinline__ float operator()(float x) const { return mul ? x * inv : x / s; }
+};
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -80,10 +90,12 @@ __device__ __forceinline__ float warp_max(float x) {
 // One CTA of 8 warps per (plane, 128-row block) of a [planes, N, 128] bf16
 // tensor: rotate every row, take the block's scale, write the e4m3 codes
 // [planes, N, 128] and the scale [planes, nblk].
+// zero_bits (may be null): block 0 of each plane also zeroes zero_bits[plane].
 __global__ void __launch_bounds__(256) attn_fp8_rows_kernel(const __nv_bfloat16 *x, uint8_t *codes, float *scales,
-                                                            int N, int nblk) {
+                                                            int N, int nblk, unsigned *zero_bits) {
   __shared__ float wmax[8];
   const int plane = blockIdx.x / nblk, blk = blockIdx.x % nblk;
+  if (zero_bits && blk == 0 && threadIdx.x == 0) zero_bits[plane] = 0u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float v[16][4];
   float amax = 0.f;
@@ -107,14 +119,15 @@ __global__ void __launch_bounds__(256) attn_fp8_rows_kernel(const __nv_bfloat16 
     v[i][1] = __fadd_rn(a1, a3);
     v[i][3] = __fsub_rn(a1, a3);
     // stride 4 ... 64: the partner lane differs in one bit; the lower lane
-    // keeps a + b, the upper b_lower - own
+    // keeps own + partner, the upper partner - own: fma(+-1, own, partner)
+    // rounds exactly as that addition or subtraction
 #pragma unroll
     for (int t = 0; t < 5; ++t) {
-      const bool upper = (lane >> t) & 1;
+      const float sg = ((lane >> t) & 1) ? -1.f : 1.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float o = __shfl_xor_sync(0xffffffffu, v[i][c], 1 << t);
-        v[i][c] = upper ? __fsub_rn(o, v[i][c]) : __fadd_rn(v[i][c], o);
+        v[i][c] = __fmaf_rn(sg, v[i][c], o);
       }
     }
 #pragma unroll
@@ -129,25 +142,30 @@ __global__ void __launch_bounds__(256) attn_fp8_rows_kernel(const __nv_bfloat16 
   float a = wmax[0];
 #pragma unroll
   for (int w = 1; w < 8; ++w) a = fmaxf(a, wmax[w]);
-  const float s = pow2_scale(a);
-  if (threadIdx.x == 0) scales[(int64_t)plane * nblk + blk] = s;
+  const InvPow2 d(pow2_exp(a));
+  if (threadIdx.x == 0) scales[(int64_t)plane * nblk + blk] = d.s;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int r = blk * BM + warp * 16 + i;
     if (r < N) {
-      const uint32_t w = pack_e4m3x2(v[i][0] / s, v[i][1] / s) | (pack_e4m3x2(v[i][2] / s, v[i][3] / s) << 16);
+      const uint32_t w = pack_e4m3x2(d(v[i][0]), d(v[i][1])) | (pack_e4m3x2(d(v[i][2]), d(v[i][3])) << 16);
       *reinterpret_cast<uint32_t *>(codes + ((int64_t)plane * N + r) * HD + lane * 4) = w;
     }
   }
 }
 
-// One CTA per (b, kv head): the V scale from max |v| over the head.
-__global__ void __launch_bounds__(256) attn_fp8_vscale_kernel(const __nv_bfloat16 *v, float *scales, int N) {
+// One CTA per (plane, 128-key block) of V: the block's max |v|, folded into
+// the head's maximum by an atomic max on its bits (non-negative floats order
+// like their bit patterns); the K rows kernel, earlier on the stream, zeroed
+// them.
+__global__ void __launch_bounds__(256) attn_fp8_vmax_kernel(const __nv_bfloat16 *v, unsigned *vmax_bits, int N,
+                                                            int nblk) {
   __shared__ float wmax[8];
-  const int64_t n8 = (int64_t)N * HD / 8;
-  const uint4 *src = reinterpret_cast<const uint4 *>(v + (int64_t)blockIdx.x * N * HD);
+  const int plane = blockIdx.x / nblk, blk = blockIdx.x % nblk;
+  const int rows = min(BN, N - blk * BN);
+  const uint4 *src = reinterpret_cast<const uint4 *>(v + ((int64_t)plane * N + (int64_t)blk * BN) * HD);
   float amax = 0.f;
-  for (int64_t i = threadIdx.x; i < n8; i += 256) {
+  for (int i = threadIdx.x; i < rows * (HD / 8); i += 256) {
     const uint4 w = src[i];
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -160,49 +178,60 @@ __global__ void __launch_bounds__(256) attn_fp8_vscale_kernel(const __nv_bfloat1
   if (threadIdx.x == 0) {
     float a = wmax[0];
     for (int w = 1; w < 8; ++w) a = fmaxf(a, wmax[w]);
-    scales[blockIdx.x] = pow2_scale(a);
+    atomicMax(vmax_bits + plane, __float_as_uint(a));
   }
+}
+
+// sv[i] = the power-of-two scale of the head maximum whose bits sv holds.
+__global__ void __launch_bounds__(256) attn_fp8_vscale_kernel(float *sv, int n) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i < n) sv[i] = pow2_scale(__uint_as_float(reinterpret_cast<unsigned *>(sv)[i]));
 }
 
 // One CTA per (plane, 128-key block): V codes e4m3(v / sv) written transposed,
 // vt[plane][d][key] with rows of nkv_pad = 128 * nblk bytes (keys >= N hold
-// code 0).
+// code 0).  Thread t converts keys 4 (t % 32) .. + 3 at head dims
+// 16 (t / 32) .. + 15 and packs each head dim's four codes into one word.
 __global__ void __launch_bounds__(256) attn_fp8_vt_kernel(const __nv_bfloat16 *v, const float *scales, uint8_t *vt,
                                                           int N, int nkv_pad, int nblk) {
-  __shared__ uint8_t tile[HD][BN + 16];  // [d][key], rows padded against bank conflicts
+  __shared__ uint32_t tile[HD][BN / 4 + 1];  // [d][key / 4], rows padded against bank conflicts
   const int plane = blockIdx.x / nblk, blk = blockIdx.x % nblk;
   const int k0 = blk * BN;
-  const float s = scales[plane];
-  // thread t converts key row r = t / 2, head-dim half (t % 2) * 64
+  // the head's max |v| (bits, see attn_fp8_vmax_kernel) -> its scale
+  const InvPow2 dv(pow2_exp(__uint_as_float(reinterpret_cast<const unsigned *>(scales)[plane])));
   {
-    const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
-    const int key = k0 + r;
-    for (int c = 0; c < 64; c += 8) {
-      const int d = h * 64 + c;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (key < N) w = *reinterpret_cast<const uint4 *>(v + ((int64_t)plane * N + key) * HD + d);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    const int kg = threadIdx.x & 31, dg = threadIdx.x >> 5;
+    uint32_t w[4][8];  // [key][bf16 pairs of the 16 head dims]
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t p = pack_e4m3x2(__uint_as_float(ws[e] << 16) / s, __uint_as_float(ws[e] & 0xffff0000u) / s);
-        tile[d + 2 * e][r] = (uint8_t)(p & 0xffu);
-        tile[d + 2 * e + 1][r] = (uint8_t)(p >> 8);
+    for (int e = 0; e < 4; ++e) {
+      const int key = k0 + 4 * kg + e;
+      uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+      if (key < N) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(v + ((int64_t)plane * N + key) * HD + 16 * dg);
+        a = src[0];
+        b = src[1];
       }
+      w[e][0] = a.x; w[e][1] = a.y; w[e][2] = a.z; w[e][3] = a.w;
+      w[e][4] = b.x; w[e][5] = b.y; w[e][6] = b.z; w[e][7] = b.w;
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        x[e] = dv(__uint_as_float((c & 1) ? (w[e][c >> 1] & 0xffff0000u) : (w[e][c >> 1] << 16)));
+      tile[16 * dg + c][kg] = pack_e4m3x2(x[0], x[1]) | (pack_e4m3x2(x[2], x[3]) << 16);
     }
   }
   __syncthreads();
   // thread t writes head-dim row d = t / 2, keys (t % 2) * 64 .. + 64, in 16-byte pieces
   {
     const int d = threadIdx.x >> 1, h = threadIdx.x & 1;
-    for (int c = 0; c < 64; c += 16) {
-      const int kk = h * 64 + c;
-      if (k0 + kk >= nkv_pad) break;
-      uint32_t w[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w[e] = (uint32_t)tile[d][kk + 4 * e] | ((uint32_t)tile[d][kk + 4 * e + 1] << 8) |
-               ((uint32_t)tile[d][kk + 4 * e + 2] << 16) | ((uint32_t)tile[d][kk + 4 * e + 3] << 24);
-      *reinterpret_cast<uint4 *>(vt + ((int64_t)plane * HD + d) * nkv_pad + k0 + kk) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int c = 0; c < 4; ++c) {
+      const int wi = h * 16 + 4 * c;
+      *reinterpret_cast<uint4 *>(vt + ((int64_t)plane * HD + d) * nkv_pad + k0 + 4 * wi) =
+          make_uint4(tile[d][wi], tile[d][wi + 1], tile[d][wi + 2], tile[d][wi + 3]);
     }
   }
 }
@@ -429,15 +458,30 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
       const int kbase = j * BN;
-      const bool full = kbase + BN <= vis_end;
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // warp-uniform: both paths end in the warp-collective tcgen05.st
+      const bool full = __all_sync(0xffffffffu, kbase + BN <= vis_end);
+      float mblk;
+      if (full) {
+        // block max of the raw scores, four chains of 3-input maxima
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < BN; ++q) {
-        const float x = __uint_as_float(sr[q >> 5][q & 31]);
-        mx[q & 3] = fmaxf(mx[q & 3], (full || kbase + q < vis_end) ? x : -INFINITY);
+        for (int q = 0; q < BN; q += 8) {
+          mx0 = max3f(mx0, __uint_as_float(sr[q >> 5][(q & 31) + 0]), __uint_as_float(sr[q >> 5][(q & 31) + 1]));
+          mx1 = max3f(mx1, __uint_as_float(sr[q >> 5][(q & 31) + 2]), __uint_as_float(sr[q >> 5][(q & 31) + 3]));
+          mx2 = max3f(mx2, __uint_as_float(sr[q >> 5][(q & 31) + 4]), __uint_as_float(sr[q >> 5][(q & 31) + 5]));
+          mx3 = max3f(mx3, __uint_as_float(sr[q >> 5][(q & 31) + 6]), __uint_as_float(sr[q >> 5][(q & 31) + 7]));
+        }
+        mblk = max3f(mx0, mx1, fmaxf(mx2, mx3)) * c;
+      } else {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int q = 0; q < BN; ++q) {
+          const float x = __uint_as_float(sr[q >> 5][q & 31]);
+          mx[q & 3] = fmaxf(mx[q & 3], (kbase + q < vis_end) ? x : -INFINITY);
+        }
+        const float ext = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        mblk = (ext == -INFINITY) ? -INFINITY : ext * c;
       }
-      const float ext = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      const float mblk = (ext == -INFINITY) ? -INFINITY : ext * c;
       const float m_new = fmaxf(m_use, mblk);
       if (__any_sync(0xffffffffu, m_new > m_use + TAU)) {
         const float alpha = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m_new);
@@ -460,22 +504,50 @@ __global__ void __launch_bounds__(THREADS, 1)
       // columns [8h, 8h + 8), all inside the first quarter, already read
       const float bias = P_SHIFT - ((m_use == -INFINITY) ? 0.f : m_use);
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      if (full) {
+        // every key visible: y on f32x2 pairs, exp2 on the MUFU
+        const uint64_t c2 = f2_pack(c, c), b2 = f2_pack(bias, bias);
+        uint64_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t pk[8];
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[8];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          float p[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int q = 32 * h + 4 * w + e;
-            const bool vis = full || kbase + q < vis_end;
-            p[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[h][4 * w + e]), c, bias)) : 0.f;
+          for (int w = 0; w < 8; ++w) {
+            const uint64_t y01 = f2_fma(f2_pack(__uint_as_float(sr[h][4 * w]), __uint_as_float(sr[h][4 * w + 1])), c2, b2);
+            const uint64_t y23 =
+                f2_fma(f2_pack(__uint_as_float(sr[h][4 * w + 2]), __uint_as_float(sr[h][4 * w + 3])), c2, b2);
+            float y0, y1, y2, y3;
+            f2_unpack(y01, y0, y1);
+            f2_unpack(y23, y2, y3);
+            const float p0 = ex2_approx(y0), p1 = ex2_approx(y1), p2 = ex2_approx(y2), p3 = ex2_approx(y3);
+            acc0 = f2_add(acc0, f2_pack(p0, p1));
+            acc1 = f2_add(acc1, f2_pack(p2, p3));
+            pk[w] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
           }
-          ls[w & 3] += (p[0] + p[1]) + (p[2] + p[3]);
-          pk[w] = pack_e4m3x2(p[0], p[1]) | (pack_e4m3x2(p[2], p[3]) << 16);
+          tmem_st8(tS + 8 * h, pk);
         }
-        tmem_st8(tS + 8 * h, pk);
+        float a0, a1, b0, b1;
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, b0, b1);
+        ls[0] = a0 + a1;
+        ls[1] = b0 + b1;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int q = 32 * h + 4 * w + e;
+              p[e] = (kbase + q < vis_end) ? ex2_approx(fmaf(__uint_as_float(sr[h][4 * w + e]), c, bias)) : 0.f;
+            }
+            ls[w & 3] += (p[0] + p[1]) + (p[2] + p[3]);
+            pk[w] = pack_e4m3x2(p[0], p[1]) | (pack_e4m3x2(p[2], p[3]) << 16);
+          }
+          tmem_st8(tS + 8 * h, pk);
+        }
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tmem_wait_st();
@@ -581,15 +653,21 @@ extern "C" int attn_fp8_quantize(const void *q, const void *k, const void *v, vo
   const auto *kb = static_cast<const __nv_bfloat16 *>(k);
   const auto *vb = static_cast<const __nv_bfloat16 *>(v);
   if (has_q) {
-    attn_fp8_rows_kernel<<<(unsigned)((int64_t)B * Hq * nqb), 256, 0, st>>>(qb, static_cast<uint8_t *>(q8), sq, Nq, nqb);
+    attn_fp8_rows_kernel<<<(unsigned)((int64_t)B * Hq * nqb), 256, 0, st>>>(qb, static_cast<uint8_t *>(q8), sq, Nq, nqb,
+                                                                              nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return record_cuda_error(e);
   }
   if (has_k) {
-    attn_fp8_rows_kernel<<<(unsigned)((int64_t)B * Hkv * nkb), 256, 0, st>>>(kb, static_cast<uint8_t *>(k8), sk, Nkv, nkb);
-    attn_fp8_vscale_kernel<<<(unsigned)(B * Hkv), 256, 0, st>>>(vb, sv, Nkv);
-    attn_fp8_vt_kernel<<<(unsigned)((int64_t)B * Hkv * nkb), 256, 0, st>>>(vb, sv, static_cast<uint8_t *>(vt8), Nkv,
-                                                                            nkv_pad, nkb);
+    // sv carries the bits of each head's max |v| until the last kernel turns
+    // them into the scales: K rows (zeroing them), V block maxima (atomic
+    // max), V codes (each block derives the scale from the maximum), scales
+    unsigned *vbits = reinterpret_cast<unsigned *>(sv);
+    const unsigned g = (unsigned)((int64_t)B * Hkv * nkb);
+    attn_fp8_rows_kernel<<<g, 256, 0, st>>>(kb, static_cast<uint8_t *>(k8), sk, Nkv, nkb, vbits);
+    attn_fp8_vmax_kernel<<<g, 256, 0, st>>>(vb, vbits, Nkv, nkb);
+    attn_fp8_vt_kernel<<<g, 256, 0, st>>>(vb, sv, static_cast<uint8_t *>(vt8), Nkv, nkv_pad, nkb);
+    attn_fp8_vscale_kernel<<<(unsigned)((B * Hkv + 255) / 256), 256, 0, st>>>(sv, B * Hkv);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return record_cuda_error(e);
   }
