@@ -580,23 +580,44 @@ __global__ void __launch_bounds__(THREADS, 1)
         // a block with masked keys (or scale <= 0): the scores are read again a
         // quarter at a time as above, and a masked key gives exactly 0.  One
         // quarter's code, looped: unrolling it measured 3 % slower overall
-        // (this kernel is sensitive to the size of its code)
+        // (this kernel is sensitive to the size of its code).  A quarter
+        // whose keys every row of the warp sees needs no test per key, and
+        // one that no row of the warp sees is not read at all (on a causal
+        // diagonal block warp w has w of the first kind and 3 - w of the
+        // second)
+        const int vis_lo = __reduce_min_sync(0xffffffffu, vis_end);
+        const int vis_hi = __reduce_max_sync(0xffffffffu, vis_end);
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
         for (int h = 0; h < 4; ++h) {
-          uint32_t cur[32];
-          tmem_ld32(tS + 32 * h, cur);
-          tmem_wait_ld();
-          reg_fence32(cur);
           const int c0 = kbase + 32 * h;
           uint32_t pk[16];
+          if (c0 >= vis_hi) {  // warp-uniform: every key hidden
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = __uint_as_float(cur[2 * i]), bb = __uint_as_float(cur[2 * i + 1]);
-            const float p0 = (c0 + 2 * i >= vis_end) ? 0.f : ex2_approx(fmaf(a, sl2, -mu));
-            const float p1 = (c0 + 2 * i + 1 >= vis_end) ? 0.f : ex2_approx(fmaf(bb, sl2, -mu));
-            ls[i & 3] += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
+            for (int i = 0; i < 16; ++i) pk[i] = 0u;
+          } else {
+            uint32_t cur[32];
+            tmem_ld32(tS + 32 * h, cur);
+            tmem_wait_ld();
+            reg_fence32(cur);
+            if (c0 + 32 <= vis_lo) {  // warp-uniform: every key visible
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float p0 = ex2_approx(fmaf(__uint_as_float(cur[2 * i]), sl2, -mu));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(cur[2 * i + 1]), sl2, -mu));
+                ls[i & 3] += p0 + p1;
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float a = __uint_as_float(cur[2 * i]), bb = __uint_as_float(cur[2 * i + 1]);
+                const float p0 = (c0 + 2 * i >= vis_end) ? 0.f : ex2_approx(fmaf(a, sl2, -mu));
+                const float p1 = (c0 + 2 * i + 1 >= vis_end) ? 0.f : ex2_approx(fmaf(bb, sl2, -mu));
+                ls[i & 3] += p0 + p1;
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+            }
           }
           tmem_st16(tS + h * 16, pk);
         }
