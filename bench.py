@@ -1,7 +1,7 @@
 """Attention-forward benchmark: device-timed TFLOPS on GB300, one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+                    [--workload NAME] [--path fwd|mask|bwd|fp8] [--no-cpu-baseline] [--no-e2e]
 
 A step is one attention forward (the whole path: every kernel attn_fwd
 launches) over one batch of the workload's seeded synthetic inputs, already
@@ -10,6 +10,11 @@ L2, outside the per-step CUDA events.  FLOPs = 4*B*Hq*Nq*Nkv*D, halved when
 causal.  Under torchrun every rank runs the full workload on its own GPU
 (weak scaling, no data-path collective); the reported time is the max over
 ranks and the value is the FLOPs of all ranks over that time.
+
+``--path`` selects what a step runs besides the default forward: the forward
+with an additive mask, the backward (FLOPs 2.5x the forward's), or the FP8
+forward (quantisation included; roofline against twice the measured bf16
+peak, the nominal e4m3/bf16 ratio).  Those lines carry no e2e or CPU leg.
 
 ``--impl reference`` times the float64 CPU oracle on the host cores instead
 (there is no other implementation of this path to run), on a bounded sample
@@ -134,6 +139,9 @@ KERNEL_SOURCES = {
     "attn_tc2_kernel": ("attn_tc2.cu",) + _COMMON_SOURCES,
     "attn_tc_kernel": ("attn_tc.cu",) + _COMMON_SOURCES,
     "attn_tcx_kernel": ("attn_tcx.cu",) + _COMMON_SOURCES,
+    "attn_bwd_dkdv_kernel": ("attn_bwd.cu",) + _COMMON_SOURCES,
+    "attn_bwd_dq_kernel": ("attn_bwd.cu",) + _COMMON_SOURCES,
+    "attn_fp8_kernel": ("attn_fp8.cu",) + _COMMON_SOURCES,
 }
 
 
@@ -325,6 +333,50 @@ def run_reference(args, w):
 METRIC = "attn fwd TFLOPS (bf16, device-timed, 1 GPU) and % of GB300 dense BF16 peak"
 
 
+PATHS = {
+    # path: (metric, dtype, what a step runs)
+    "fwd": (None, "bf16", "attn_fwd: one forward"),
+    "mask": ("attn fwd with an additive mask TFLOPS (bf16, device-timed, 1 GPU)", "bf16",
+             "attn_fwd_masked with one [Nq, Nkv] bf16 mask shared by every batch and head"),
+    "bwd": ("attn bwd TFLOPS (bf16, device-timed, 1 GPU; FLOPs = 2.5 x the forward's)", "bf16",
+            "attn_bwd: Delta/LSE prep, dK/dV kernel, dQ kernel"),
+    "fp8": ("attn fwd FP8 TFLOPS (e4m3 operands, device-timed, 1 GPU)", "e4m3",
+            "attn_fp8_quantize of bf16 q, k, v then attn_fwd_fp8"),
+}
+
+
+def make_step(path, w, dev, dq, dk, dv, out, lse, stream):
+    """The callable one step runs, its FLOPs and its algorithmic HBM bytes."""
+    from exact_attention_attn_gb300 import attn_bwd, attn_fp8_quantize, attn_fwd, attn_fwd_fp8
+    if path == "fwd":
+        return (lambda: attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream),
+                w.flops(), w.hbm_bytes())
+    if path == "mask":
+        g = torch.Generator().manual_seed(w.seed + 7)
+        pad = (w.Nkv + 7) // 8 * 8
+        store = (torch.randn((w.Nq, pad), generator=g) * 2.0).to(torch.bfloat16).to(dev)
+        mask = store[:, :w.Nkv]
+        return (lambda: attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream,
+                                 mask=mask),
+                w.flops(), w.hbm_bytes() + w.Nq * w.Nkv * 2)
+    if path == "bwd":
+        attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream)
+        g = torch.Generator().manual_seed(w.seed + 1000)
+        dout = torch.randn(out.shape, generator=g).to(torch.bfloat16).to(dev)
+        gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+        qo = w.B * w.Hq * w.Nq * w.D * 2
+        kv = w.B * w.Hkv * w.Nkv * w.D * 2
+        byts = 3 * qo + 2 * kv + w.B * w.Hq * w.Nq * 4 + qo + 2 * kv   # q, o, dO, k, v, lse in; dq, dk, dv out
+        return (lambda: attn_bwd(dq, dk, dv, out, lse, dout, scale=w.scale, causal=w.causal, stream=stream,
+                                 dq=gq, dk=gk, dv=gv),
+                2.5 * w.flops(), byts)
+    if path == "fp8":
+        return (lambda: attn_fwd_fp8(attn_fp8_quantize(dq, dk, dv, stream=stream), scale=w.scale, causal=w.causal,
+                                     out=out, lse=lse, stream=stream),
+                w.flops(), w.hbm_bytes())
+    raise ValueError(path)
+
+
 def run_ours(args, w):
     from exact_attention_attn_gb300 import attn_fwd, attn_fwd_host, attn_fwd_status, load_library
 
@@ -344,9 +396,10 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    step, flops, alg_bytes = make_step(args.path, w, dev, dq, dk, dv, out, lse, stream)
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
-        attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream)
+        step()
     torch.cuda.synchronize(dev)
     st = attn_fwd_status(stream)
     if st != 0:
@@ -362,7 +415,7 @@ def run_ours(args, w):
     for i in range(args.steps):
         flush.fill_(i & 0xFF)                      # L2 flush, outside the events
         starts[i].record(stream)
-        attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream)
+        step()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     barrier(ws)
@@ -375,31 +428,36 @@ def run_ours(args, w):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = statistics.mean(step_ms)
     ms = reduce_max(ms_local, ws, dev)
-    flops = w.flops()
     value = flops * max(ws, 1) / (ms * 1e-3) / 1e12
 
     # roofline of the dominant (here: the only) kernel of a step: the tensor
     # pipe where the workload's FLOPs per algorithmic byte exceed the
     # machine's ridge (peak FLOP/s / HBM B/s), else HBM
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_label = f"{peak_src} bf16 dense burst"
+    if args.path == "fp8":  # the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+        peak *= 2.0
+        peak_label = f"{peak_src} bf16 dense burst x 2 (nominal e4m3 / bf16 ratio)"
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     achieved = flops / (ms_local * 1e-3) / 1e12
-    achieved_gbs = w.hbm_bytes() / (ms_local * 1e-3) / 1e9
-    traffic, traffic_kernel = recorded_traffic(w.name)
-    common = {"traffic": traffic, "algorithmic_flops_per_launch": flops, "algorithmic_hbm_bytes_per_launch": w.hbm_bytes(),
+    achieved_gbs = alg_bytes / (ms_local * 1e-3) / 1e9
+    traffic, traffic_kernel = recorded_traffic(w.name) if args.path == "fwd" else (None, None)
+    common = {"traffic": traffic, "algorithmic_flops_per_launch": flops, "algorithmic_hbm_bytes_per_launch": alg_bytes,
               "kernel": traffic_kernel}
-    if flops / w.hbm_bytes() > peak * 1e3 / hbm_peak:
+    if args.path != "fwd":
+        common["scope"] = "the whole step (" + PATHS[args.path][2] + ")"
+    if flops / alg_bytes > peak * 1e3 / hbm_peak:
         roofline = dict({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_source": f"{peak_src} bf16 dense burst",
+                         "frac": achieved / peak, "peak_source": peak_label,
                          "achieved_hbm_gbs": achieved_gbs}, **common)
     else:
         roofline = dict({"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved_gbs / hbm_peak, "peak_source": f"{peak_src} HBM copy",
                          "achieved_tflops": achieved, "us_per_launch": ms_local * 1e3}, **common)
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers (the forward path)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.path == "fwd":
         pq, pk, pv = q.pin_memory(), k.pin_memory(), v.pin_memory()
         po = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         pl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
@@ -418,7 +476,7 @@ def run_ours(args, w):
                "steps": n_e2e}
 
     cpu = None
-    if rank == 0 and ws <= 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws <= 1 and not args.no_cpu_baseline and args.path == "fwd":
         tf, heads, dt, nrows = time_oracle(w, q, k, v, budget_s=args.cpu_seconds)
         threads = blas_threads() or cpu_cores()
         cpu = {"value": tf, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
@@ -427,14 +485,15 @@ def run_ours(args, w):
             cpu["single_thread"] = single_thread_oracle(w, args.cpu_seconds)
 
     if rank == 0:
+        metric, dtype, _ = PATHS[args.path]
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": max(ws, 1), "steps": args.steps,
+            "metric": metric or METRIC, "value": value, "unit": "TFLOPS", "n_gpus": max(ws, 1), "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": bench_config(w, ws),
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": dict(bench_config(w, ws), **({"path": args.path} if args.path != "fwd" else {})),
             "pct_of_peak": 100.0 * value / max(ws, 1) / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * kernels_per_call(w),
+            "gpu_launches": args.steps * kernels_per_call(w, args.path),
             "clocks": clocks, "timed_wall_s": t_wall,
             "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)},
         }
@@ -444,7 +503,12 @@ def run_ours(args, w):
     return 0
 
 
-def kernels_per_call(w) -> int:
+def kernels_per_call(w, path: str = "fwd") -> int:
+    """Kernels of ours one step launches."""
+    if path == "bwd":
+        return 3          # prep, dK/dV, dQ
+    if path == "fp8":
+        return 6          # Q rows, K rows, V maxima, V codes, V scales, attention
     from exact_attention_attn_gb300.binding import attn_fwd_plan
     return attn_fwd_plan(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal)["launches"]
 
@@ -456,6 +520,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--path", default="fwd", choices=list(PATHS),
+                    help="what a step runs: the forward (default), the masked forward, the backward, the FP8 forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -115,26 +115,30 @@ __device__ __forceinline__ void init_bars(BwdBars *bars) {
 
 // ---------------------------------------------------------------- prep
 
-// One warp per padded query row: Delta = sum_d dO O (fp32), LSE in log2 units.
+// Delta = sum_d dO O (fp32) and LSE in log2 units for every padded query
+// row.  D / 8 threads per row, each with one 16-byte load of O and of dO,
+// summed by shuffles within the row's lanes: 256 / (D / 8) rows per CTA.
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= (int64_t)p.B * p.Hq * p.nq_pad) return;
-  const int64_t bh = row / p.nq_pad;
-  const int i = (int)(row % p.nq_pad);
+  const int tpr = p.D / 8;  // threads per row: 8 (D = 64) or 16 (D = 128)
+  const int64_t row = (int64_t)blockIdx.x * (256 / tpr) + threadIdx.x / tpr;
+  const int part = threadIdx.x % tpr;
+  const bool in = row < (int64_t)p.B * p.Hq * p.nq_pad;
+  const int64_t bh = in ? row / p.nq_pad : 0;
+  const int i = in ? (int)(row % p.nq_pad) : p.nq_pad;
   float acc = 0.f;
-  if (i < p.Nq) {
-    const int64_t base = (bh * p.Nq + i) * p.D;
-    for (int c = lane * 2; c < p.D; c += 64) {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(p.o + base + c);
-      const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162 *>(p.dout + base + c);
-      acc = fmaf(__low2float(a), __low2float(d), acc);
-      acc = fmaf(__high2float(a), __high2float(d), acc);
+  if (in && i < p.Nq) {
+    const int64_t base = (bh * p.Nq + i) * p.D + part * 8;
+    const uint4 a = *reinterpret_cast<const uint4 *>(p.o + base);
+    const uint4 d = *reinterpret_cast<const uint4 *>(p.dout + base);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, dv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      acc = fmaf(__uint_as_float(av[c] << 16), __uint_as_float(dv[c] << 16), acc);
+      acc = fmaf(__uint_as_float(av[c] & 0xffff0000u), __uint_as_float(dv[c] & 0xffff0000u), acc);
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
+  for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (in && part == 0) {
     float l2 = INFINITY;
     if (i < p.Nq) {
       const float l = p.lse[bh * p.Nq + i];
@@ -639,7 +643,8 @@ cudaError_t launch_bwd_d(const BwdParams &prm, const __nv_bfloat16 *q, const __n
     if (e != cudaSuccess) return e;
     attr_set[device].store(1, std::memory_order_release);
   }
-  const int64_t prep_blocks = ((int64_t)prm.B * prm.Hq * prm.nq_pad + 7) / 8;
+  const int64_t prep_rows_per_cta = 256 / (D / 8);
+  const int64_t prep_blocks = ((int64_t)prm.B * prm.Hq * prm.nq_pad + prep_rows_per_cta - 1) / prep_rows_per_cta;
   const int64_t g_dkdv = (int64_t)prm.B * prm.Hkv * ((prm.Nkv + BT - 1) / BT);
   const int64_t g_dq = (int64_t)prm.B * prm.Hq * ((prm.Nq + BT - 1) / BT);
   if (prep_blocks > 0x7fffffffLL || g_dkdv > 0x7fffffffLL || g_dq > 0x7fffffffLL)
