@@ -20,18 +20,21 @@
 //         dP^T = V dO^T on the tensor cores, P^T and dS^T by the math warps
 //         (one key row per thread) written back to TMEM as bf16, then
 //         dV += P^T dO and dK += dS^T Q with P^T / dS^T read from TMEM;
-//   dq    one CTA per (b, q head, 128-row query tile), looping over key
-//         blocks: S = Q K^T, dP = dO V^T, dS by the math warps (one query
-//         row per thread), dQ += dS K.
+//   dq    one CTA per (b, q head, pair of 128-row query tiles), looping
+//         over key blocks shared by both tiles: S = Q K^T, dP = dO V^T in
+//         the same TMEM columns once S has been read, dS by the math warps
+//         (one query row per thread), dQ += dS K, the two tiles interleaved.
 // The split into a key-stationary and a query-stationary kernel recomputes
 // S and dP once more (7 block products instead of 5) but needs no atomic
 // accumulation of dQ and gives the same bits on every run.
 //
-// CTA = 6 warps: 0-3 math (TMEM lanes 32w..32w+31), 4 TMA producer (one
-// thread), 5 TMEM allocator and MMA issuer (one thread).
+// dkdv CTA = 6 warps: 0-3 math (TMEM lanes 32w..32w+31), 4 TMA producer (one
+// thread), 5 TMEM allocator and MMA issuer (one thread); dq CTA = 10 warps:
+// 0-7 math (tile w / 4), 8 the two producers, 9 the MMA issuer.
 //
 // TMEM columns, dkdv: S^T/P^T [0,128), dP^T/dS^T [128,256), dV [256,256+D),
-// dK [256+D, 256+2D); dq: S [0,128), dP/dS [128,256), dQ [256,256+D).
+// dK [256+D, 256+2D); dq: S_t/dP_t/dS_t [128t, 128t+128), dQ_t
+// [256 + Dt, 256 + Dt + D).
 // P (bf16 pairs) overwrites the first 64 columns of S a quarter at a time
 // after the quarter it lands on has been read; the same for dS over dP.
 //
@@ -330,12 +333,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       // key kk_row is visible to query q iff kk_row <= q + shift (causal)
       const int qmin = kk_row - shift;  // first visible query
       float pr[BT];
+      uint32_t qb[2][32];
+      tmem_ld32(tS, qb[0]);
+      tmem_wait_ld();
+      reg_fence32(qb[0]);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        uint32_t cur[32];
-        tmem_ld32(tS + 32 * h, cur);
-        tmem_wait_ld();
-        reg_fence32(cur);
+        uint32_t(&cur)[32] = qb[h & 1];
+        if (h < 3) tmem_ld32(tS + 32 * (h + 1), qb[(h + 1) & 1]);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -348,18 +353,23 @@ __global__ void __launch_bounds__(THREADS, 1)
           pk[i >> 1] = pack_bf16x2(pr[c], pr[c + 1]);
         }
         tmem_st16(tS + 16 * h, pk);
+        if (h < 3) {
+          tmem_wait_ld();
+          reg_fence32(qb[(h + 1) & 1]);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, jj & 1, abortf, limit))) { ok = false; break; }
       tc_fence_after();
+      tmem_ld32(tDP, qb[0]);
+      tmem_wait_ld();
+      reg_fence32(qb[0]);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        uint32_t cur[32];
-        tmem_ld32(tDP + 32 * h, cur);
-        tmem_wait_ld();
-        reg_fence32(cur);
+        uint32_t(&cur)[32] = qb[h & 1];
+        if (h < 3) tmem_ld32(tDP + 32 * (h + 1), qb[(h + 1) & 1]);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -371,6 +381,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           pk[i >> 1] = pack_bf16x2(ds0, ds1);
         }
         tmem_st16(tDP + 16 * h, pk);
+        if (h < 3) {
+          tmem_wait_ld();
+          reg_fence32(qb[(h + 1) & 1]);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -417,39 +431,94 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---------------------------------------------------------------- dQ
 
+constexpr int DQ_THREADS = 320;  // warps 0-7 math (tile = warp / 4), 8 producers, 9 MMA
+constexpr int DQ_WARP_LOAD = 8, DQ_WARP_MMA = 9;
+constexpr int DQ_MAX_KST = 4, DQ_MAX_VST = 4;
+
+struct DqBars {
+  uint64_t q_full;  // Q_t and dO_t of both tiles (one producer each)
+  uint64_t k_full[DQ_MAX_KST], k_empty[DQ_MAX_KST];
+  uint64_t v_full[DQ_MAX_VST], v_empty[DQ_MAX_VST];
+  uint64_t s_full[2], dp_full[2];  // MMA -> math
+  uint64_t s_free[2], ds_full[2];  // math -> MMA
+  uint64_t o_done[2];
+  uint64_t done;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+struct DqLayout {
+  int kst, vst;
+  uint32_t off_k, off_v, off_bar;
+  int smem;
+};
+
+// Two 128-row query tiles per CTA share every K and V block; tile t keeps
+// S_t, then dP_t, then dS_t (bf16 over its first 64 columns) in TMEM columns
+// [128t, 128t + 128) and accumulates dQ_t in [256 + D t, 256 + D t + D).  Per
+// key block j the MMA thread issues dP0, dP1 (each once its tile's math warps
+// have read S), then dQ0 and S0 of the next block, dQ1 and S1 of the next
+// block (each dQ once its tile's dS is written), so that one tile's math
+// overlaps the other tile's products.  P stays in the math warps' registers
+// (bf16) between S and dP.
 template <int D>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                       const BwdParams p) {
+                       const BwdParams p, const DqLayout lay) {
   constexpr int NC = D / 64;
   constexpr int TILE = NC * CHUNK_BYTES;
-  constexpr int STAGE = 2 * TILE;  // K block, V block
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t *sq = smem, *sdo = smem + TILE;
-  uint8_t *ring = smem + 2 * TILE;
-  BwdBars *bars = reinterpret_cast<BwdBars *>(ring + NST * STAGE);
+  uint8_t *sq = smem, *sdo = smem + 2 * TILE;  // tile t at + t * TILE
+  uint8_t *sk = smem + lay.off_k, *sv = smem + lay.off_v;
+  DqBars *bars = reinterpret_cast<DqBars *>(smem + lay.off_bar);
   volatile int *abortf = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t limit = p.wait_limit_ns;
 
-  // ---- work unit: (b, hq) fastest, then query tile (causal: heaviest first)
+  // ---- work unit: (b, hq) fastest, then tile pair (causal: heaviest first)
   const int BH = p.B * p.Hq;
   const int nqt = (p.Nq + BT - 1) / BT;
-  const int bh = blockIdx.x % BH, tt = blockIdx.x / BH;
-  const int tile = p.causal ? nqt - 1 - tt : tt;
+  const int npairs = (nqt + 1) / 2;
+  const int bh = blockIdx.x % BH, t_idx = blockIdx.x / BH;
+  const int pair = p.causal ? npairs - 1 - t_idx : t_idx;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
-  const int q0 = tile * BT;
   const int shift = p.Nkv - p.Nq;
-  int kv_end = p.Nkv;
-  if (p.causal) kv_end = max(0, min(p.Nkv, q0 + BT - 1 + shift + 1));
-  const int nblk = (kv_end + BT - 1) / BT;
+  int nblk_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int q0 = (2 * pair + t) * BT;
+    int kv_end = p.Nkv;
+    if (p.causal) kv_end = max(0, min(p.Nkv, q0 + BT - 1 + shift + 1));
+    nblk_t[t] = (q0 < p.Nq) ? (kv_end + BT - 1) / BT : 0;
+  }
+  const int nblk = max(nblk_t[0], nblk_t[1]);
 
-  if (tid == 0) init_bars(bars);
-  if (warp == WARP_MMA) {
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 2);
+    for (int i = 0; i < lay.kst; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < lay.vst; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->dp_full[t], 1);
+      mbar_init(&bars->s_free[t], 128);
+      mbar_init(&bars->ds_full[t], 128);
+      mbar_init(&bars->o_done[t], 1);
+    }
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == DQ_WARP_MMA) {
     tmem_alloc(&bars->tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
@@ -458,40 +527,52 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
 
-  if (warp == WARP_LOAD) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && nblk > 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars->fixed_full, 2 * TILE);
-      tma_load_4d(sq, &tm_q, &bars->fixed_full, 0, q0, 0, bh);
-      tma_load_4d(sdo, &tm_do, &bars->fixed_full, 0, q0, 0, bh);
+  if (warp == DQ_WARP_LOAD) {
+    // ------------------------------------------------------------ producers
+    // lane 0: Q_0, dO_0, then the K ring; lane 1: Q_1, dO_1, then the V ring
+    if (lane < 2 && nblk > 0) {
+      const bool is_k = lane == 0;
+      const int t = lane;
+      const int nst = is_k ? lay.kst : lay.vst;
+      uint8_t *ring = is_k ? sk : sv;
+      const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
+      tma_prefetch_desc(tm);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * TILE);
+      tma_load_4d(sq + t * TILE, &tm_q, &bars->q_full, 0, (2 * pair + t) * BT, 0, bh);
+      tma_load_4d(sdo + t * TILE, &tm_do, &bars->q_full, 0, (2 * pair + t) * BT, 0, bh);
       bool ok = true;
       int issued = 0;
       for (int j = 0; j < nblk; ++j) {
-        const int s = j % NST;
-        if (!mbar_wait(&bars->empty[s], ((j / NST) & 1) ^ 1, abortf, limit)) { ok = false; break; }
-        uint8_t *st = ring + s * STAGE;
-        mbar_arrive_expect_tx(&bars->full[s], STAGE);
-        tma_load_4d(st, &tm_k, &bars->full[s], 0, j * BT, 0, bkv);
-        tma_load_4d(st + TILE, &tm_v, &bars->full[s], 0, j * BT, 0, bkv);
+        const int s = j % nst;
+        uint64_t *empty = is_k ? &bars->k_empty[s] : &bars->v_empty[s];
+        uint64_t *full = is_k ? &bars->k_full[s] : &bars->v_full[s];
+        if (!mbar_wait(empty, ((j / nst) & 1) ^ 1, abortf, limit)) { ok = false; break; }
+        mbar_arrive_expect_tx(full, TILE);
+        tma_load_4d(ring + s * TILE, tm, full, 0, j * BT, 0, bkv);
         ++issued;
       }
-      if (!ok) raise_abort(bars, p.status);
-      mbar_wait_drain(&bars->fixed_full, 0, limit);
-      for (int i = issued > NST ? issued - NST : 0; i < issued; ++i)
-        mbar_wait_drain(&bars->full[i % NST], (i / NST) & 1, limit);
+      if (!ok) {
+        atomicCAS(p.status, 0, kStatusTimeout);
+        *reinterpret_cast<volatile int *>(&bars->abort) = 1;
+      }
+      mbar_wait_drain(&bars->q_full, 0, limit);
+      for (int i = issued > nst ? issued - nst : 0; i < issued; ++i)
+        mbar_wait_drain(is_k ? &bars->k_full[i % nst] : &bars->v_full[i % nst], (i / nst) & 1, limit);
     }
-  } else if (warp == WARP_MMA) {
+  } else if (warp == DQ_WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nblk > 0) {
       const uint32_t idesc_s = idesc_bf16(BT, BT, 0, 0);
       const uint32_t idesc_o = idesc_bf16(BT, D, 0, 1);
-      constexpr uint64_t kChunkD = CHUNK_BYTES >> 4, kStageD = (uint64_t)STAGE >> 4;
+      constexpr uint64_t kChunkD = CHUNK_BYTES >> 4, kTileD = (uint64_t)TILE >> 4;
       const uint64_t qd = smem_desc(smem_u32(sq), 16, 1024), dod = smem_desc(smem_u32(sdo), 16, 1024);
-      const uint64_t k_km = smem_desc(smem_u32(ring), 16, 1024);
-      const uint64_t v_km = smem_desc(smem_u32(ring + TILE), 16, 1024);
-      const uint64_t k_mn = smem_desc(smem_u32(ring), CHUNK_BYTES, 1024);
+      const uint64_t k_km = smem_desc(smem_u32(sk), 16, 1024), k_mn = smem_desc(smem_u32(sk), CHUNK_BYTES, 1024);
+      const uint64_t v_km = smem_desc(smem_u32(sv), 16, 1024);
+      auto abort_all = [&]() {
+        atomicCAS(p.status, 0, kStatusTimeout);
+        *reinterpret_cast<volatile int *>(&bars->abort) = 1;
+      };
+      // A [128 x D] K-major tile times B [128 x D] K-major block into TMEM col
       auto issue_nt = [&](uint32_t col, uint64_t ad, uint64_t bd) {
 #pragma unroll
         for (int c = 0; c < NC; ++c)
@@ -500,98 +581,147 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_ss(tmem + col, ad + (uint64_t)(c * kChunkD + kk * 2), bd + (uint64_t)(c * kChunkD + kk * 2), idesc_s,
                    (c | kk) != 0);
       };
-      bool ok = mbar_wait(&bars->fixed_full, 0, abortf, limit);
-      if (ok) ok = mbar_wait(&bars->full[0], 0, abortf, limit);
+      auto act = [&](int t, int j) { return j < nblk_t[t]; };
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
+      bool ok = mbar_wait(&bars->q_full, 0, abortf, limit);
+      if (ok) ok = mbar_wait(&bars->k_full[0], 0, abortf, limit);
       if (ok) {
         tc_fence_after();
-        issue_nt(TM_S, qd, k_km);
-        mma_commit(&bars->s_full);
-        issue_nt(TM_DP, dod, v_km);
-        mma_commit(&bars->dp_full);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (act(t, 0)) {
+            issue_nt(BT * t, qd + (uint64_t)t * kTileD, k_km);
+            mma_commit(&bars->s_full[t]);
+          }
       }
       for (int j = 0; j < nblk && ok; ++j) {
-        const int s = j % NST, s1 = (j + 1) % NST;
-        const uint64_t so = (uint64_t)s * kStageD, so1 = (uint64_t)s1 * kStageD;
-        // S of the next block once the math warps have read this one
-        if (j + 1 < nblk) {
-          if (!mbar_wait(&bars->s_free, j & 1, abortf, limit)) { ok = false; break; }
-          if (!mbar_wait(&bars->full[s1], ((j + 1) / NST) & 1, abortf, limit)) { ok = false; break; }
-          tc_fence_after();
-          issue_nt(TM_S, qd, k_km + so1);
-          mma_commit(&bars->s_full);
-        }
-        // dQ += dS K (dS from TMEM over dP)
-        if (!mbar_wait(&bars->ds_full, j & 1, abortf, limit)) { ok = false; break; }
-        tc_fence_after();
+        // dP_t = dO_t V_j^T once tile t's math warps have read S_t
+        if (!mbar_wait(&bars->v_full[vs], vph, abortf, limit)) { ok = false; break; }
 #pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)
-          mma_ts(tmem + TM_ACC, tmem + TM_DP + kk * 8, k_mn + so + (uint64_t)(kk * (2048 >> 4)), idesc_o,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->empty[s]);
-        if (j + 1 < nblk) {
-          issue_nt(TM_DP, dod, v_km + so1);
-          mma_commit(&bars->dp_full);
+        for (int t = 0; t < 2; ++t) {
+          if (!act(t, j)) continue;
+          if (!mbar_wait(&bars->s_free[t], j & 1, abortf, limit)) { ok = false; break; }
+          tc_fence_after();
+          issue_nt(BT * t, dod + (uint64_t)t * kTileD, v_km + (uint64_t)vs * kTileD);
+          mma_commit(&bars->dp_full[t]);
         }
+        if (!ok) break;
+        mma_commit(&bars->v_empty[vs]);
+        if (++vs == lay.vst) {
+          vs = 0;
+          vph ^= 1u;
+        }
+        // dQ_t += dS_t K_j once dS_t is written, then S_t of the next block
+        int ks1 = ks + 1;
+        uint32_t kph1 = kph;
+        if (ks1 == lay.kst) {
+          ks1 = 0;
+          kph1 ^= 1u;
+        }
+        if (j + 1 < nblk && !mbar_wait(&bars->k_full[ks1], kph1, abortf, limit)) { ok = false; break; }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!act(t, j)) continue;
+          if (!mbar_wait(&bars->ds_full[t], j & 1, abortf, limit)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BT / 16; ++kk)
+            mma_ts(tmem + TM_ACC + D * t, tmem + BT * t + kk * 8, k_mn + (uint64_t)ks * kTileD + (uint64_t)(kk * (2048 >> 4)),
+                   idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          if (j == nblk_t[t] - 1) mma_commit(&bars->o_done[t]);
+          if (act(t, j + 1)) {
+            issue_nt(BT * t, qd + (uint64_t)t * kTileD, k_km + (uint64_t)ks1 * kTileD);
+            mma_commit(&bars->s_full[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bars->k_empty[ks]);
+        ks = ks1;
+        kph = kph1;
       }
-      if (!ok) raise_abort(bars, p.status);
-      mma_commit(&bars->o_done);
+      if (!ok) abort_all();
       mma_commit(&bars->done);
-      if (!mbar_wait_drain(&bars->done, 0, limit)) raise_abort(bars, p.status);
+      if (!mbar_wait_drain(&bars->done, 0, limit)) abort_all();
     }
   } else {
     // ------------------------------------------------------------ math: one query row per thread
-    const int row = tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_base + TM_S, tDP = tmem + lane_base + TM_DP;
-    const int qi = q0 + row;
+    const int t = warp >> 2;
+    const int row = tid & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tR = tmem + lane_base + BT * t;
+    const int qi = (2 * pair + t) * BT + row;
+    const int nb = nblk_t[t];
     const int64_t vrow = (int64_t)bh * p.nq_pad + qi;  // padded rows hold lse2 = +inf
-    const float lse2 = p.lse2[vrow], delta = p.delta[vrow];
+    const bool in_pad = qi < p.nq_pad;
+    const float lse2 = in_pad ? p.lse2[vrow] : INFINITY, delta = in_pad ? p.delta[vrow] : 0.f;
     const int vis_end = p.causal ? min(p.Nkv, qi + shift + 1) : p.Nkv;  // keys [0, vis_end) visible
     const float sl2 = p.scale * kLog2e;
     bool ok = true;
-    for (int j = 0; j < nblk; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, abortf, limit))) { ok = false; break; }
+    for (int j = 0; j < nb; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abortf, limit))) { ok = false; break; }
       tc_fence_after();
       const int kbase = j * BT;
-      float pr[BT];
+      // the scores a quarter (32 keys) at a time, the next quarter's load in
+      // flight while this one is turned into P
+      uint32_t pb[BT / 2];  // P as bf16 pairs
+      uint32_t qb[2][32];
+      tmem_ld32(tR, qb[0]);
+      tmem_wait_ld();
+      reg_fence32(qb[0]);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        uint32_t cur[32];
-        tmem_ld32(tS + 32 * h, cur);
-        tmem_wait_ld();
-        reg_fence32(cur);
+        uint32_t(&cur)[32] = qb[h & 1];
+        if (h < 3) tmem_ld32(tR + 32 * (h + 1), qb[(h + 1) & 1]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = 32 * h + i;
-          pr[c] = (kbase + c < vis_end) ? ex2_approx(fmaf(__uint_as_float(cur[i]), sl2, -lse2)) : 0.f;
+        for (int i = 0; i < 32; i += 2) {
+          const int c = kbase + 32 * h + i;
+          const float p0 = (c < vis_end) ? ex2_approx(fmaf(__uint_as_float(cur[i]), sl2, -lse2)) : 0.f;
+          const float p1 = (c + 1 < vis_end) ? ex2_approx(fmaf(__uint_as_float(cur[i + 1]), sl2, -lse2)) : 0.f;
+          pb[16 * h + (i >> 1)] = pack_bf16x2(p0, p1);
+        }
+        if (h < 3) {
+          tmem_wait_ld();
+          reg_fence32(qb[(h + 1) & 1]);
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->s_free);
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full, j & 1, abortf, limit))) { ok = false; break; }
+      mbar_arrive(&bars->s_free[t]);
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dp_full[t], j & 1, abortf, limit))) { ok = false; break; }
       tc_fence_after();
+      // dS a quarter at a time the same way; quarter h lands in columns
+      // [16h, 16h + 16), already read, while the load in flight reads further on
+      tmem_ld32(tR, qb[0]);
+      tmem_wait_ld();
+      reg_fence32(qb[0]);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        uint32_t cur[32];
-        tmem_ld32(tDP + 32 * h, cur);
-        tmem_wait_ld();
-        reg_fence32(cur);
+        uint32_t(&cur)[32] = qb[h & 1];
+        if (h < 3) tmem_ld32(tR + 32 * (h + 1), qb[(h + 1) & 1]);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const int c = 32 * h + i;
-          pk[i >> 1] = pack_bf16x2(pr[c] * (__uint_as_float(cur[i]) - delta),
-                                   pr[c + 1] * (__uint_as_float(cur[i + 1]) - delta));
+          const uint32_t w = pb[16 * h + (i >> 1)];
+          pk[i >> 1] = pack_bf16x2(__uint_as_float(w << 16) * (__uint_as_float(cur[i]) - delta),
+                                   __uint_as_float(w & 0xffff0000u) * (__uint_as_float(cur[i + 1]) - delta));
         }
-        tmem_st16(tDP + 16 * h, pk);
+        tmem_st16(tR + 16 * h, pk);
+        if (h < 3) {
+          tmem_wait_ld();
+          reg_fence32(qb[(h + 1) & 1]);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full);
+      mbar_arrive(&bars->ds_full[t]);
     }
-    if (!ok) raise_abort(bars, p.status);
-    if (ok && nblk > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, abortf, limit))) {
-      raise_abort(bars, p.status);
+    if (!ok) {
+      atomicCAS(p.status, 0, kStatusTimeout);
+      *reinterpret_cast<volatile int *>(&bars->abort) = 1;
+    }
+    if (ok && nb > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], 0, abortf, limit))) {
+      atomicCAS(p.status, 0, kStatusTimeout);
+      *reinterpret_cast<volatile int *>(&bars->abort) = 1;
       ok = false;
     }
     if (ok) {
@@ -600,8 +730,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t rr[32];
-        if (nblk > 0) {
-          tmem_ld32(tmem + lane_base + TM_ACC + cc * 32, rr);
+        if (nb > 0) {
+          tmem_ld32(tmem + lane_base + TM_ACC + D * t + cc * 32, rr);
           tmem_wait_ld();
           reg_fence32(rr);
         } else {
@@ -615,7 +745,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == WARP_MMA) {
+  if (warp == DQ_WARP_MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -623,12 +753,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int D>
+DqLayout dq_layout() {
+  constexpr int TILE = (D / 64) * CHUNK_BYTES;
+  DqLayout L;
+  const int avail = kSmemMax - 2048 - 4 * TILE;  // Q and dO of both tiles resident
+  int slots = avail / TILE;                       // K and V ring slots
+  L.kst = slots >= 4 ? (slots / 2 > DQ_MAX_KST ? DQ_MAX_KST : slots / 2) : 2;
+  L.vst = slots - L.kst > DQ_MAX_VST ? DQ_MAX_VST : slots - L.kst;
+  L.off_k = 4 * TILE;
+  L.off_v = L.off_k + L.kst * TILE;
+  L.off_bar = L.off_v + L.vst * TILE;
+  L.smem = (int)L.off_bar + (int)sizeof(DqBars) + 1024;
+  return L;
+}
+
+template <int D>
 cudaError_t launch_bwd_d(const BwdParams &prm, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                          const __nv_bfloat16 *v, int device, cudaStream_t st) {
   constexpr int TILE = (D / 64) * CHUNK_BYTES;
   constexpr int SM_DKDV = 2 * TILE + NST * (2 * TILE + VEC_BYTES) + (int)sizeof(BwdBars) + 1024;
-  constexpr int SM_DQ = 2 * TILE + NST * 2 * TILE + (int)sizeof(BwdBars) + 1024;
-  static_assert(SM_DKDV <= kSmemMax && SM_DQ <= kSmemMax, "shared memory plan too large");
+  static_assert(SM_DKDV <= kSmemMax, "shared memory plan too large");
+  const DqLayout dql = dq_layout<D>();
+  if (dql.kst < 2 || dql.vst < 1 || dql.smem > kSmemMax) return cudaErrorInvalidConfiguration;
   CUtensorMap tq, tdo, tk, tv;
   if (!make_block_map(&tq, q, D, prm.Nq, prm.B * prm.Hq, BT)) return cudaErrorInvalidValue;
   if (!make_block_map(&tdo, prm.dout, D, prm.Nq, prm.B * prm.Hq, BT)) return cudaErrorInvalidValue;
@@ -646,7 +792,7 @@ cudaError_t launch_bwd_d(const BwdParams &prm, const __nv_bfloat16 *q, const __n
   const int64_t prep_rows_per_cta = 256 / (D / 8);
   const int64_t prep_blocks = ((int64_t)prm.B * prm.Hq * prm.nq_pad + prep_rows_per_cta - 1) / prep_rows_per_cta;
   const int64_t g_dkdv = (int64_t)prm.B * prm.Hkv * ((prm.Nkv + BT - 1) / BT);
-  const int64_t g_dq = (int64_t)prm.B * prm.Hq * ((prm.Nq + BT - 1) / BT);
+  const int64_t g_dq = (int64_t)prm.B * prm.Hq * (((prm.Nq + BT - 1) / BT + 1) / 2);
   if (prep_blocks > 0x7fffffffLL || g_dkdv > 0x7fffffffLL || g_dq > 0x7fffffffLL)
     return cudaErrorInvalidConfiguration;
   attn_bwd_prep_kernel<<<(unsigned)prep_blocks, 256, 0, st>>>(prm);
@@ -654,7 +800,7 @@ cudaError_t launch_bwd_d(const BwdParams &prm, const __nv_bfloat16 *q, const __n
   if (e != cudaSuccess) return e;
   attn_bwd_dkdv_kernel<D><<<(unsigned)g_dkdv, THREADS, SM_DKDV, st>>>(tq, tdo, tk, tv, prm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  attn_bwd_dq_kernel<D><<<(unsigned)g_dq, THREADS, SM_DQ, st>>>(tq, tdo, tk, tv, prm);
+  attn_bwd_dq_kernel<D><<<(unsigned)g_dq, DQ_THREADS, dql.smem, st>>>(tq, tdo, tk, tv, prm, dql);
   return cudaGetLastError();
 }
 
