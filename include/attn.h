@@ -263,7 +263,9 @@ ATTN_API int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *
  * the whole GQA group, another dQ per query tile over the keys).  A
  * stream-ordered scratch of 2 * B * Hq * ceil(Nq / 128) * 128 * 4 bytes is
  * taken from the library's pool (see attn_fwd_splitkv); ATTN_ERR_NOMEM if it
- * cannot be had.  The additive mask of attn_fwd_masked has no backward here.
+ * cannot be had.  CUDA graphs: as attn_fwd (while the stream is captured the
+ * scratch becomes a graph memory node).  The additive mask of
+ * attn_fwd_masked has no backward here.
  */
 ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
                       const float *lse, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Nq, int Nkv,
@@ -297,7 +299,8 @@ ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o
  * D must be 128; attn_fwd_fp8 also needs a finite scale > 0 (ATTN_ERR_ARG
  * otherwise).  Every pointer is a device pointer owned by the caller, 16-byte
  * aligned; sizes, causal masking (bottom-right), rows with no key, GQA,
- * asynchrony and errors are as attn_fwd.  No key-range splits.
+ * asynchrony, errors and CUDA-graph capture are as attn_fwd (neither call
+ * allocates).  No key-range splits.
  */
 ATTN_API int attn_fp8_quantize(const void *q, const void *k, const void *v, void *q8, void *k8, void *vt8,
                                float *sq, float *sk, float *sv, int B, int Hq, int Hkv, int Nq, int Nkv, int D,

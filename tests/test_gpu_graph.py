@@ -72,3 +72,86 @@ def test_graph_case_paths():
     names = {c: attn_fwd_plan(*c[:7])["path_name"] for c in GRAPH_CASES}
     assert names[GRAPH_CASES[5]] == "tc_splitkv"
     assert all(n in ("tc", "tc_splitkv") for n in names.values())
+
+
+def _replay_check(capture, direct, refill):
+    """Warm up, capture one call into a graph, then twice: write new inputs
+    into the captured buffers, replay, and compare with a direct call."""
+    capture()  # first-use setup outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs = capture()
+    for seed in (11, 22):
+        refill(seed)
+        for t in outs:
+            t.fill_(float("nan")) if t.is_floating_point() else None
+        g.replay()
+        refs = direct()
+        torch.cuda.synchronize()
+        for a, b in zip(outs, refs):
+            assert torch.equal(a, b), seed
+    assert attn_fwd_status() == 0
+
+
+@pytest.mark.parametrize("D", [128, 512])
+def test_graph_masked_forward(D):
+    from exact_attention_attn_gb300 import attn_fwd
+    B, Hq, Hkv, Nq, Nkv = 1, 2, 1, 200, 300
+    q, k, v = (t.cuda() for t in make_qkv(B, Hq, Hkv, Nq, Nkv, D, seed=5))
+    mask = torch.zeros((Nq, 304), dtype=torch.bfloat16, device="cuda")[:, :Nkv]
+    out = torch.empty((B, Hq, Nq, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device="cuda")
+
+    def refill(seed):
+        q2, k2, v2 = make_qkv(B, Hq, Hkv, Nq, Nkv, D, seed=seed)
+        q.copy_(q2), k.copy_(k2), v.copy_(v2)
+        mask.copy_(torch.randn((Nq, Nkv), generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16))
+
+    _replay_check(lambda: attn_fwd(q, k, v, causal=True, out=out, lse=lse, mask=mask),
+                  lambda: attn_fwd(q, k, v, causal=True, mask=mask), refill)
+
+
+def test_graph_backward():
+    from exact_attention_attn_gb300 import attn_bwd
+    B, Hq, Hkv, Nq, Nkv, D = 1, 4, 2, 300, 300, 128
+    q, k, v = (t.cuda() for t in make_qkv(B, Hq, Hkv, Nq, Nkv, D, seed=6))
+    o, lse = attn_fwd(q, k, v, causal=True)
+    do = torch.randn_like(o)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def refill(seed):
+        q2, k2, v2 = make_qkv(B, Hq, Hkv, Nq, Nkv, D, seed=seed)
+        q.copy_(q2), k.copy_(k2), v.copy_(v2)
+        attn_fwd(q, k, v, causal=True, out=o, lse=lse)
+
+    _replay_check(lambda: attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv),
+                  lambda: attn_bwd(q, k, v, o, lse, do, causal=True), refill)
+
+
+def test_graph_fp8_forward():
+    from exact_attention_attn_gb300 import attn_fp8_quantize, attn_fwd_fp8
+    B, Hq, Hkv, Nq, Nkv, D = 1, 4, 2, 300, 333, 128
+    q, k, v = (t.cuda() for t in make_qkv(B, Hq, Hkv, Nq, Nkv, D, seed=7))
+    qz = attn_fp8_quantize(q, k, v)
+    out = torch.empty((B, Hq, Nq, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device="cuda")
+    import ctypes
+    from exact_attention_attn_gb300.binding import load_library
+    lib = load_library()
+
+    def quantize_into():  # quantisation into the same buffers every time
+        rc = lib.attn_fp8_quantize(q.data_ptr(), k.data_ptr(), v.data_ptr(), qz["q8"].data_ptr(), qz["k8"].data_ptr(),
+                                   qz["vt8"].data_ptr(), qz["sq"].data_ptr(), qz["sk"].data_ptr(), qz["sv"].data_ptr(),
+                                   B, Hq, Hkv, Nq, Nkv, D, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0
+
+    def capture():
+        quantize_into()
+        return attn_fwd_fp8(qz, causal=True, out=out, lse=lse)
+
+    def refill(seed):
+        q2, k2, v2 = make_qkv(B, Hq, Hkv, Nq, Nkv, D, seed=seed)
+        q.copy_(q2), k.copy_(k2), v.copy_(v2)
+
+    _replay_check(capture, lambda: attn_fwd_fp8(attn_fp8_quantize(q, k, v), causal=True), refill)
