@@ -229,29 +229,60 @@ def oracle_rows(w):
     return sample_rows(w.Nq, w.sample_rows, w.seed) if w.sample_rows else None
 
 
-def time_oracle(w, q, k, v, budget_s: float, max_heads: int | None = None):
-    """Run the oracle head by head over the workload (on each head's sampled
-    rows where the workload samples) until budget_s seconds have passed (at
-    least one head).  Returns (TFLOPS, heads, seconds, rows per head).  The
-    FLOPs credited to a head are the workload's FLOPs per head times the
-    share of its rows that ran (a per-row linear extrapolation when rows are
-    sampled)."""
+def path_host_inputs(path: str, w):
+    """Seeded host tensors a path adds to q, k and v: the additive mask
+    ([Nq, Nkv] bf16, a view of a row store padded to a multiple of 8
+    columns) of the masked path and the upstream gradient dO of the
+    backward.  Both legs of the bench (kernels and oracle) use these."""
+    extra = {}
+    if path == "mask":
+        g = torch.Generator().manual_seed(w.seed + 7)
+        pad = (w.Nkv + 7) // 8 * 8
+        extra["mask"] = (torch.randn((w.Nq, pad), generator=g) * 2.0).to(torch.bfloat16)[:, :w.Nkv]
+    if path == "bwd":
+        g = torch.Generator().manual_seed(w.seed + 1000)
+        extra["dout"] = torch.randn((w.B, w.Hq, w.Nq, w.D), generator=g).to(torch.bfloat16)
+    return extra
+
+
+def time_oracle(w, q, k, v, budget_s: float, max_heads: int | None = None, path: str = "fwd",
+                extra: dict | None = None):
+    """Run the oracle of `path` head by head over the workload until
+    budget_s seconds have passed (at least one head).  Returns (TFLOPS,
+    heads, seconds, rows per head).
+
+    fwd, mask, fp8: the forward of one (b, hq) head on its sampled rows
+    where the workload samples (fp8 first rotates and quantises that head's
+    Q, K and V as the FP8 path does); the FLOPs credited are the workload's
+    FLOPs per head times the share of rows that ran (a per-row linear
+    extrapolation when rows are sampled).  bwd: the whole backward of one
+    head (every row: dK and dV need them all), credited 2.5 x the forward's
+    FLOPs per head."""
     import oracle
     B, Hq = w.B, w.Hq
     heads = [(b, h) for b in range(B) for h in range(Hq)]
     if max_heads:
         heads = heads[:max_heads]
-    rows = oracle_rows(w)
+    rows = None if path == "bwd" else oracle_rows(w)
     nrows = w.Nq if rows is None else len(rows)
-    per_head_flops = w.flops() / (B * Hq) * nrows / w.Nq
+    per_head_flops = (2.5 if path == "bwd" else 1.0) * w.flops() / (B * Hq) * nrows / w.Nq
+    mask = None if path != "mask" else to_f64(extra["mask"])
     done = 0
     t0 = time.perf_counter()
     group = w.Hq // w.Hkv
     for b, h in heads:
-        qh = to_f64(q[b, h])
-        kh = to_f64(k[b, h // group])
-        vh = to_f64(v[b, h // group])
-        oracle.attention_head(qh, kh, vh, w.scale, w.causal, rows)
+        kvh = h // group
+        if path == "fp8":
+            (qd, kd, vd), _ = oracle.fp8.fp8_inputs(to_f64(q[b:b + 1, h:h + 1]),
+                                                    to_f64(k[b:b + 1, kvh:kvh + 1]),
+                                                    to_f64(v[b:b + 1, kvh:kvh + 1]))
+            oracle.attention_head(qd[0, 0], kd[0, 0], vd[0, 0], w.scale, w.causal, rows)
+        elif path == "bwd":
+            oracle.attention_backward_head(to_f64(q[b, h]), to_f64(k[b, kvh]), to_f64(v[b, kvh]),
+                                           to_f64(extra["dout"][b, h]), w.scale, w.causal)
+        else:
+            oracle.attention_head(to_f64(q[b, h]), to_f64(k[b, kvh]), to_f64(v[b, kvh]), w.scale, w.causal,
+                                  rows, mask)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -259,7 +290,13 @@ def time_oracle(w, q, k, v, budget_s: float, max_heads: int | None = None):
     return per_head_flops * done / dt / 1e12, done, dt, nrows
 
 
-def oracle_sample_text(w, heads, dt, nrows, threads):
+def oracle_sample_text(w, heads, dt, nrows, threads, path="fwd"):
+    if path != "fwd":
+        what = {"mask": "the masked forward", "fp8": "FWHT rotation + e4m3 quantisation of Q, K, V, then the forward",
+                "bwd": "the whole backward (dQ, dK, dV; FLOPs credited 2.5 x the forward's)"}[path]
+        rows = f"{nrows} seeded rows" if nrows < w.Nq else f"all {w.Nq} rows"
+        return (f"{what} on {rows} of each of {heads} (b,hq) heads (of {w.B * w.Hq}) of {w.name}; "
+                f"float64 numpy on {threads} host thread(s), {dt:.1f} s")
     what = (f"{nrows} seeded rows of each of {heads} (b,hq) heads (of {w.B * w.Hq}) of {w.name}; TFLOPS credit "
             f"each head with its FLOPs x {nrows}/{w.Nq} (per-row linear extrapolation)" if nrows < w.Nq else
             f"{heads} of {w.B * w.Hq} (b,hq) heads of {w.name}, all {w.Nq} rows each")
@@ -303,25 +340,27 @@ def run_reference(args, w):
     if ws > 1 and rank != 0:
         return 0
     q, k, v = make_workload_inputs(w)
+    extra = path_host_inputs(args.path, w)
     per_step_budget = 5.0
     for _ in range(args.warmup):
-        time_oracle(w, q, k, v, budget_s=0.0, max_heads=1)
+        time_oracle(w, q, k, v, budget_s=0.0, max_heads=1, path=args.path, extra=extra)
     vals, heads_total, secs, nrows = [], 0, 0.0, w.Nq
     for _ in range(args.steps):
-        tf, heads, dt, nrows = time_oracle(w, q, k, v, budget_s=per_step_budget)
+        tf, heads, dt, nrows = time_oracle(w, q, k, v, budget_s=per_step_budget, path=args.path, extra=extra)
         vals.append(tf)
         heads_total += heads
         secs += dt
     value = statistics.mean(vals)
     cores = blas_threads() or cpu_cores()
-    sample = (oracle_sample_text(w, heads_total, secs, nrows, cores) +
+    sample = (oracle_sample_text(w, heads_total, secs, nrows, cores, args.path) +
               f"; {args.steps} steps, each stopping after {per_step_budget:.0f} s")
-    flops_per_head = w.flops() / (w.B * w.Hq)
+    flops_per_head = (2.5 if args.path == "bwd" else 1.0) * w.flops() / (w.B * w.Hq)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 0 if ws <= 1 else ws,
+        "impl": "reference", "metric": PATHS[args.path][0] or METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": 0 if ws <= 1 else ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": bench_config(w, ws),
+        "config": dict(bench_config(w, ws), **({"path": args.path} if args.path != "fwd" else {})),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "flops_per_head": flops_per_head,
@@ -345,36 +384,70 @@ PATHS = {
 }
 
 
-def make_step(path, w, dev, dq, dk, dv, out, lse, stream):
-    """The callable one step runs, its FLOPs and its algorithmic HBM bytes."""
+def make_step(path, w, dev, dq, dk, dv, out, lse, stream, extra):
+    """The callable one step runs, its FLOPs, its algorithmic HBM bytes, and
+    for the end-to-end leg the (host, device) input pairs a user copies in
+    and the device results a user reads back."""
     from exact_attention_attn_gb300 import attn_bwd, attn_fp8_quantize, attn_fwd, attn_fwd_fp8
+    ins, outs = [], [out, lse]
     if path == "fwd":
-        return (lambda: attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream),
-                w.flops(), w.hbm_bytes())
+        step = lambda: attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse,  # noqa: E731
+                                stream=stream)
+        return step, w.flops(), w.hbm_bytes(), ins, outs
     if path == "mask":
-        g = torch.Generator().manual_seed(w.seed + 7)
-        pad = (w.Nkv + 7) // 8 * 8
-        store = (torch.randn((w.Nq, pad), generator=g) * 2.0).to(torch.bfloat16).to(dev)
+        host_store = extra["mask"].as_strided((w.Nq, (w.Nkv + 7) // 8 * 8), extra["mask"].stride())
+        store = host_store.to(dev)
         mask = store[:, :w.Nkv]
-        return (lambda: attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream,
-                                 mask=mask),
-                w.flops(), w.hbm_bytes() + w.Nq * w.Nkv * 2)
+        ins = [(host_store, store)]
+        step = lambda: attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse,  # noqa: E731
+                                stream=stream, mask=mask)
+        return step, w.flops(), w.hbm_bytes() + w.Nq * w.Nkv * 2, ins, outs
     if path == "bwd":
         attn_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream)
-        g = torch.Generator().manual_seed(w.seed + 1000)
-        dout = torch.randn(out.shape, generator=g).to(torch.bfloat16).to(dev)
+        dout = extra["dout"].to(dev)
         gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
         qo = w.B * w.Hq * w.Nq * w.D * 2
         kv = w.B * w.Hkv * w.Nkv * w.D * 2
         byts = 3 * qo + 2 * kv + w.B * w.Hq * w.Nq * 4 + qo + 2 * kv   # q, o, dO, k, v, lse in; dq, dk, dv out
-        return (lambda: attn_bwd(dq, dk, dv, out, lse, dout, scale=w.scale, causal=w.causal, stream=stream,
-                                 dq=gq, dk=gk, dv=gv),
-                2.5 * w.flops(), byts)
+        ins = [(out.cpu(), out), (lse.cpu(), lse), (extra["dout"], dout)]
+        step = lambda: attn_bwd(dq, dk, dv, out, lse, dout, scale=w.scale, causal=w.causal,  # noqa: E731
+                                stream=stream, dq=gq, dk=gk, dv=gv)
+        return step, 2.5 * w.flops(), byts, ins, [gq, gk, gv]
     if path == "fp8":
-        return (lambda: attn_fwd_fp8(attn_fp8_quantize(dq, dk, dv, stream=stream), scale=w.scale, causal=w.causal,
-                                     out=out, lse=lse, stream=stream),
-                w.flops(), w.hbm_bytes())
+        step = lambda: attn_fwd_fp8(attn_fp8_quantize(dq, dk, dv, stream=stream),  # noqa: E731
+                                    scale=w.scale, causal=w.causal, out=out, lse=lse, stream=stream)
+        return step, w.flops(), w.hbm_bytes(), ins, outs
     raise ValueError(path)
+
+
+def e2e_path(step, flops, ins, outs, q, k, v, dq, dk, dv, stream, n, ws, dev):
+    """A path's metric end to end through the Python API: every step copies
+    its inputs from pinned host memory to the device, runs the path, and
+    copies its results back to pinned host memory, timed on the host."""
+    pairs = [(t.pin_memory(), d) for t, d in [(q, dq), (k, dk), (v, dv)] + ins]
+    backs = [(torch.empty(d.shape, dtype=d.dtype, pin_memory=True), d) for d in outs]
+
+    def once():
+        with torch.cuda.stream(stream):
+            for h, d in pairs:
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in backs:
+                h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        once()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        once()
+    dt = reduce_max((time.perf_counter() - t0) / n, ws, dev)
+    return {"value": flops * max(ws, 1) / dt / 1e12, "unit": "TFLOPS",
+            "h2d_bytes_per_step": int(sum(h.numel() * h.element_size() for h, _ in pairs)),
+            "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for h, _ in backs)),
+            "ms_per_step": dt * 1e3, "steps": n, "api": "pinned host -> device copies, the path's Python calls, "
+            "device -> pinned host copies, one stream"}
 
 
 def run_ours(args, w):
@@ -396,7 +469,8 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    step, flops, alg_bytes = make_step(args.path, w, dev, dq, dk, dv, out, lse, stream)
+    extra = path_host_inputs(args.path, w)
+    step, flops, alg_bytes, e2e_ins, e2e_outs = make_step(args.path, w, dev, dq, dk, dv, out, lse, stream, extra)
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
         step()
@@ -474,14 +548,17 @@ def run_ours(args, w):
                "h2d_bytes_per_step": int(q.numel() * 2 + k.numel() * 2 + v.numel() * 2),
                "d2h_bytes_per_step": int(out.numel() * 2 + lse.numel() * 4), "ms_per_step": dt * 1e3,
                "steps": n_e2e}
+    elif not args.no_e2e:
+        e2e = e2e_path(step, flops, e2e_ins, e2e_outs, q, k, v, dq, dk, dv, stream, max(3, min(args.steps, 20)),
+                       ws, dev)
 
     cpu = None
-    if rank == 0 and ws <= 1 and not args.no_cpu_baseline and args.path == "fwd":
-        tf, heads, dt, nrows = time_oracle(w, q, k, v, budget_s=args.cpu_seconds)
+    if rank == 0 and ws <= 1 and not args.no_cpu_baseline:
+        tf, heads, dt, nrows = time_oracle(w, q, k, v, budget_s=args.cpu_seconds, path=args.path, extra=extra)
         threads = blas_threads() or cpu_cores()
         cpu = {"value": tf, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-               "sample": oracle_sample_text(w, heads, dt, nrows, threads)}
-        if w.sample_rows == 0:  # the two small workloads: also on one host thread
+               "sample": oracle_sample_text(w, heads, dt, nrows, threads, args.path)}
+        if w.sample_rows == 0 and args.path == "fwd":  # the two small workloads: also on one host thread
             cpu["single_thread"] = single_thread_oracle(w, args.cpu_seconds)
 
     if rank == 0:

@@ -1,4 +1,4 @@
-"""Float64 CPU oracle for exact attention forward (test infrastructure only).
+"""Float64 CPU oracle for exact attention: forward, additive mask, backward, FP8 inputs (test infrastructure only).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  The product path never does.

@@ -44,3 +44,27 @@ def test_traffic_row_gated_by_code_hash(tmp_path, monkeypatch):
     assert bench.recorded_traffic("wl")[0] == 12345.0
     k.write_text(k.read_text() + "\nstatic int later_code = 1;\n")
     assert bench.recorded_traffic("wl") == (None, None)
+
+
+def test_oracle_leg_of_every_path():
+    # each path's CPU leg runs one head of a tiny workload through its oracle
+    # and credits that head's FLOPs (2.5 x the forward's for the backward)
+    from exact_attention_attn_gb300.workloads import Workload, make_workload_inputs
+    w = Workload("tiny_gqa_causal", B=1, Hq=2, Hkv=1, Nq=72, Nkv=72, D=64, causal=True, seed=5)
+    q, k, v = make_workload_inputs(w)
+    for path in bench.PATHS:
+        extra = bench.path_host_inputs(path, w)
+        tf, heads, dt, nrows = bench.time_oracle(w, q, k, v, budget_s=0.0, path=path, extra=extra)
+        assert heads == 1 and nrows == w.Nq and tf > 0
+        assert abs(tf * dt * 1e12 - (2.5 if path == "bwd" else 1.0) * w.flops() / 2) < 1e-6 * w.flops()
+        assert f"1 (b,hq) heads" in bench.oracle_sample_text(w, heads, dt, nrows, 1, path) or path == "fwd"
+
+
+def test_mask_store_is_padded_to_eight_columns():
+    # the masked path's mask is a [Nq, Nkv] view of a store whose rows are
+    # multiples of 8 elements (16 bytes), as attn_fwd_masked requires
+    from exact_attention_attn_gb300.workloads import Workload
+    w = Workload("tiny", B=1, Hq=1, Hkv=1, Nq=5, Nkv=13, D=64, causal=False, seed=1)
+    m = bench.path_host_inputs("mask", w)["mask"]
+    assert tuple(m.shape) == (5, 13) and m.stride() == (16, 1)
+    assert set(bench.path_host_inputs("bwd", w)) == {"dout"} and bench.path_host_inputs("fwd", w) == {}
