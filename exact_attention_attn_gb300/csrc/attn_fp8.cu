@@ -31,6 +31,7 @@
 // Since (Q H)(K H)^T = Q K^T, the result approximates exact attention on
 // the original inputs; it equals exact attention on the dequantised inputs
 // up to the rounding of P to e4m3 and fp32 accumulation.
+#include <limits.h>
 #include <math.h>
 #include <string.h>
 
@@ -87,70 +88,146 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
-// One CTA of 8 warps per (plane, 128-row block) of a [planes, N, 128] bf16
-// tensor: rotate every row, take the block's scale, write the e4m3 codes
-// [planes, N, 128] and the scale [planes, nblk].
-// zero_bits (may be null): block 0 of each plane also zeroes zero_bits[plane].
-__global__ void __launch_bounds__(256) attn_fp8_rows_kernel(const __nv_bfloat16 *x, uint8_t *codes, float *scales,
-                                                            int N, int nblk, unsigned *zero_bits) {
-  __shared__ float wmax[8];
-  const int plane = blockIdx.x / nblk, blk = blockIdx.x % nblk;
-  if (zero_bits && blk == 0 && threadIdx.x == 0) zero_bits[plane] = 0u;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float v[16][4];
-  float amax = 0.f;
+// Rotation and block quantisation of a [planes, N, 128] bf16 tensor: rotate
+// every row, take the scale of each 128-row block, write the e4m3 codes
+// [planes, N, 128] and the scales [planes, nblk].  The units (plane, block)
+// are dealt to the CTAs round-robin; a CTA of 128 threads copies its next
+// unit into the second of two shared-memory buffers while it works on the
+// current one.  Thread t owns row t of a unit: the unit is copied with
+// coalesced 16-byte copies (rows past N read as zeros), chunk c of row r at
+//     r * 256 + (c / 8) * 128 + ((c % 8) ^ (r % 8)) * 16,
+// so that 8 consecutive threads reading chunk c of their own rows touch all
+// 32 banks once; every butterfly then runs in the thread's registers on
+// packed fp32 pairs, and the codes leave through the same kind of layout with
+// coalesced 16-byte stores.
+// zero_bits (may be null): the CTA that takes block 0 of a plane also zeroes
+// zero_bits[plane].
+constexpr int ROW_THREADS = BM;
+constexpr int ROW_CTAS_PER_SM = 3;
+constexpr int ROW_BUF = BM * HD * 2;  // one unit of bf16 rows
+constexpr int ROW_SMEM = 2 * ROW_BUF;
+
+// Wait until at most the most recent cp.async group of this thread is pending.
+__device__ __forceinline__ void cp_async_wait_all_but_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+__device__ __forceinline__ void rows_copy(uint32_t buf, const uint8_t *src, int rows, int tid) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int r = blk * BM + warp * 16 + i;
-    if (r < N) {
-      const uint2 w = *reinterpret_cast<const uint2 *>(x + ((int64_t)plane * N + r) * HD + lane * 4);
-      v[i][0] = __uint_as_float(w.x << 16);
-      v[i][1] = __uint_as_float(w.x & 0xffff0000u);
-      v[i][2] = __uint_as_float(w.y << 16);
-      v[i][3] = __uint_as_float(w.y & 0xffff0000u);
+  for (int j = 0; j < ROW_BUF / 16 / ROW_THREADS; ++j) {
+    const int i = j * ROW_THREADS + tid, r = i >> 4, c = i & 15;  // chunk i = 16 r + c of the unit
+    const bool in = r < rows;
+    cp_async16(buf + r * 256 + (c >> 3) * 128 + (((c & 7) ^ (r & 7)) << 4), src + (in ? (int64_t)i * 16 : 0),
+               in ? 16u : 0u);
+  }
+  cp_async_commit();
+}
+
+__global__ void __launch_bounds__(ROW_THREADS, ROW_CTAS_PER_SM)
+    attn_fp8_rows_kernel(const __nv_bfloat16 *x, uint8_t *codes, float *scales, int N, int nblk, int nunits,
+                         unsigned *zero_bits) {
+  extern __shared__ __align__(128) uint8_t rows_smem[];
+  __shared__ float wmax[ROW_THREADS / 32];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t smem_s = smem_u32(rows_smem);
+  const uint64_t kM1 = f2_pack(-1.f, -1.f), kNZ = f2_pack(-0.f, -0.f), kC = f2_pack(kInvSqrtD, kInvSqrtD);
+  auto unit_rows = [&](int u) { return min(BM, N - (u % nblk) * BM); };  // >= 1: block < nblk
+  auto unit_src = [&](int u) {
+    return reinterpret_cast<const uint8_t *>(x + ((int64_t)(u / nblk) * N + (int64_t)(u % nblk) * BM) * HD);
+  };
+  int unit = blockIdx.x, buf = 0;
+  if (unit < nunits) rows_copy(smem_s, unit_src(unit), unit_rows(unit), tid);
+  for (; unit < nunits; unit += gridDim.x, buf ^= 1) {
+    const int plane = unit / nblk, blk = unit % nblk, rows = unit_rows(unit);
+    if (zero_bits && blk == 0 && tid == 0) zero_bits[plane] = 0u;
+    const int next = unit + gridDim.x;
+    if (next < nunits) {
+      rows_copy(smem_s + (buf ^ 1) * ROW_BUF, unit_src(next), unit_rows(next), tid);
+      cp_async_wait_all_but_1();
     } else {
-      v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
+      cp_async_wait_all();
     }
-    // butterflies of stride 1 and 2 inside the lane (elements 4 lane .. 4 lane + 3)
-    float a0 = __fadd_rn(v[i][0], v[i][1]), a1 = __fsub_rn(v[i][0], v[i][1]);
-    float a2 = __fadd_rn(v[i][2], v[i][3]), a3 = __fsub_rn(v[i][2], v[i][3]);
-    v[i][0] = __fadd_rn(a0, a2);
-    v[i][2] = __fsub_rn(a0, a2);
-    v[i][1] = __fadd_rn(a1, a3);
-    v[i][3] = __fsub_rn(a1, a3);
-    // stride 4 ... 64: the partner lane differs in one bit; the lower lane
-    // keeps own + partner, the upper partner - own: fma(+-1, own, partner)
-    // rounds exactly as that addition or subtraction
+    __syncthreads();
+    uint8_t *tb = rows_smem + buf * ROW_BUF;
+    uint64_t p[HD / 2];  // p[j] = elements (2j, 2j + 1) of this thread's row
+    const uint8_t *mine = tb + tid * 256;
 #pragma unroll
-    for (int t = 0; t < 5; ++t) {
-      const float sg = ((lane >> t) & 1) ? -1.f : 1.f;
+    for (int c = 0; c < 16; ++c) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(mine + (c >> 3) * 128 + (((c & 7) ^ (tid & 7)) << 4));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float o = __shfl_xor_sync(0xffffffffu, v[i][c], 1 << t);
-        v[i][c] = __fmaf_rn(sg, v[i][c], o);
+      for (int e = 0; e < 4; ++e) p[4 * c + e] = f2_pack(__uint_as_float(ws[e] << 16), __uint_as_float(ws[e] & 0xffff0000u));
+    }
+    // butterflies of stride 1, 2, ..., 64 in that order: the lower element
+    // keeps lo + hi, the upper lo - hi, each rounded once (stride 1 inside a
+    // pair; from stride 2 on, two butterflies per packed add and fma(-1, hi, lo))
+#pragma unroll
+    for (int j = 0; j < HD / 2; ++j) {
+      float lo, hi;
+      f2_unpack(p[j], lo, hi);
+      p[j] = f2_pack(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
+    }
+#pragma unroll
+    for (int h = 1; h < HD / 2; h <<= 1) {
+#pragma unroll
+      for (int j = 0; j < HD / 2; ++j) {
+        if ((j & h) == 0) {
+          const uint64_t lo = p[j], hi = p[j + h];
+          p[j] = f2_add(lo, hi);
+          p[j + h] = f2_fma(kM1, hi, lo);
+        }
       }
     }
+    // times 1/sqrt(D), rounded once (adding -0 keeps the sign of a zero product)
+    float amax = 0.f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      v[i][c] = __fmul_rn(v[i][c], kInvSqrtD);
-      amax = fmaxf(amax, fabsf(v[i][c]));
+    for (int j = 0; j < HD / 2; ++j) {
+      p[j] = f2_fma(p[j], kC, kNZ);
+      float lo, hi;
+      f2_unpack(p[j], lo, hi);
+      amax = max3f(amax, fabsf(lo), fabsf(hi));
     }
-  }
-  amax = warp_max(amax);
-  if (lane == 0) wmax[warp] = amax;
-  __syncthreads();
-  float a = wmax[0];
+    amax = warp_max(amax);
+    if ((tid & 31) == 0) wmax[warp] = amax;
+    __syncthreads();  // also: every thread has read its row out of the buffer
+    float a = wmax[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) a = fmaxf(a, wmax[w]);
-  const InvPow2 d(pow2_exp(a));
-  if (threadIdx.x == 0) scales[(int64_t)plane * nblk + blk] = d.s;
+    for (int w = 1; w < ROW_THREADS / 32; ++w) a = fmaxf(a, wmax[w]);
+    const InvPow2 d(pow2_exp(a));
+    if (tid == 0) scales[(int64_t)plane * nblk + blk] = d.s;
+    if (d.mul) {
+      const uint64_t inv = f2_pack(d.inv, d.inv);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int r = blk * BM + warp * 16 + i;
-    if (r < N) {
-      const uint32_t w = pack_e4m3x2(d(v[i][0]), d(v[i][1])) | (pack_e4m3x2(d(v[i][2]), d(v[i][3])) << 16);
-      *reinterpret_cast<uint32_t *>(codes + ((int64_t)plane * N + r) * HD + lane * 4) = w;
+      for (int j = 0; j < HD / 2; ++j) p[j] = f2_fma(p[j], inv, kNZ);  // exact: a power of two, normal result
+    } else {
+#pragma unroll
+      for (int j = 0; j < HD / 2; ++j) {
+        float lo, hi;
+        f2_unpack(p[j], lo, hi);
+        p[j] = f2_pack(lo / d.s, hi / d.s);
+      }
     }
+    // codes of this row: 8 chunks of 16 elements, chunk c at tid * 128 + ((c ^ (tid % 8)) * 16)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v0, v1, v2, v3;
+        f2_unpack(p[8 * c + 2 * e], v0, v1);
+        f2_unpack(p[8 * c + 2 * e + 1], v2, v3);
+        w[e] = pack_e4m3x2(v0, v1) | (pack_e4m3x2(v2, v3) << 16);
+      }
+      *reinterpret_cast<uint4 *>(tb + tid * 128 + ((c ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+    uint8_t *dst = codes + ((int64_t)plane * N + (int64_t)blk * BM) * HD;
+#pragma unroll
+    for (int j = 0; j < BM * HD / 16 / ROW_THREADS; ++j) {
+      const int i = j * ROW_THREADS + tid, r = i >> 3, c = i & 7;  // chunk i = 8 r + c of the codes
+      if (r < rows)
+        *reinterpret_cast<uint4 *>(dst + (int64_t)i * 16) =
+            *reinterpret_cast<const uint4 *>(tb + r * 128 + ((c ^ (r & 7)) << 4));
+    }
+    __syncthreads();  // the buffer's codes are out before the next copy into it
   }
 }
 
@@ -622,6 +699,22 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// CTAs of a rows launch: at most ROW_CTAS_PER_SM per SM, one per unit below that.
+unsigned rows_grid(int64_t units, int sms) {
+  const int64_t g = (int64_t)ROW_CTAS_PER_SM * sms;
+  return (unsigned)(units < g ? units : g);
+}
+
+// The rows kernel's 64 KB of dynamic shared memory, allowed once per device.
+cudaError_t rows_ready(int device) {
+  static std::atomic<int> done[64];
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  if (done[device].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(attn_fp8_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ROW_SMEM);
+  if (e == cudaSuccess) done[device].store(1, std::memory_order_release);
+  return e;
+}
+
 int fp8_sizes_ok(int B, int Hq, int Hkv, int Nq, int Nkv, int D) {
   const int rc = check_problem(B, Hq, Hkv, Nq, Nkv, D, 0);
   if (rc != ATTN_OK) return rc;
@@ -649,12 +742,16 @@ extern "C" int attn_fp8_quantize(const void *q, const void *k, const void *v, vo
   if ((rc = current_device(&device, &sms, &status)) != ATTN_OK) return rc;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int nqb = (Nq + BM - 1) / BM, nkb = (Nkv + BN - 1) / BN, nkv_pad = nkb * BN;
+  // one rows unit per (plane, 128-row block); the V kernels take one CTA per unit
+  if ((int64_t)B * Hq * nqb > INT_MAX || (int64_t)B * Hkv * nkb > INT_MAX) return ATTN_ERR_ARG;
+  if (const cudaError_t e = rows_ready(device); e != cudaSuccess) return record_cuda_error(e);
   const auto *qb = static_cast<const __nv_bfloat16 *>(q);
   const auto *kb = static_cast<const __nv_bfloat16 *>(k);
   const auto *vb = static_cast<const __nv_bfloat16 *>(v);
   if (has_q) {
-    attn_fp8_rows_kernel<<<(unsigned)((int64_t)B * Hq * nqb), 256, 0, st>>>(qb, static_cast<uint8_t *>(q8), sq, Nq, nqb,
-                                                                              nullptr);
+    const int64_t units = (int64_t)B * Hq * nqb;
+    attn_fp8_rows_kernel<<<rows_grid(units, sms), ROW_THREADS, ROW_SMEM, st>>>(
+        qb, static_cast<uint8_t *>(q8), sq, Nq, nqb, (int)units, nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return record_cuda_error(e);
   }
@@ -664,7 +761,8 @@ extern "C" int attn_fp8_quantize(const void *q, const void *k, const void *v, vo
     // max), V codes (each block derives the scale from the maximum), scales
     unsigned *vbits = reinterpret_cast<unsigned *>(sv);
     const unsigned g = (unsigned)((int64_t)B * Hkv * nkb);
-    attn_fp8_rows_kernel<<<g, 256, 0, st>>>(kb, static_cast<uint8_t *>(k8), sk, Nkv, nkb, vbits);
+    attn_fp8_rows_kernel<<<rows_grid(g, sms), ROW_THREADS, ROW_SMEM, st>>>(kb, static_cast<uint8_t *>(k8), sk, Nkv,
+                                                                          nkb, (int)g, vbits);
     attn_fp8_vmax_kernel<<<g, 256, 0, st>>>(vb, vbits, Nkv, nkb);
     attn_fp8_vt_kernel<<<g, 256, 0, st>>>(vb, sv, static_cast<uint8_t *>(vt8), Nkv, nkv_pad, nkb);
     attn_fp8_vscale_kernel<<<(unsigned)((B * Hkv + 255) / 256), 256, 0, st>>>(sv, B * Hkv);

@@ -56,6 +56,22 @@ def test_quantisation_matches_oracle_bit_for_bit(shape):
     assert nqb == (Nq + 127) // 128
 
 
+def test_quantisation_many_units_bit_for_bit():
+    # more (head, 128-row block) units than the rotation kernel keeps resident
+    # (three CTAs per SM), so each CTA walks several units through both of its
+    # buffers; ragged last blocks on both sides
+    B, Hq, Hkv, Nq, Nkv = 1, 8, 8, 8192 + 37, 8192 - 5
+    q, k, v = make_qkv(B, Hq, Hkv, Nq, Nkv, 128, seed=11, amp=2.0)
+    q[:, :, ::97, :3] *= 30
+    qz = attn_fp8_quantize(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    (qd, kd, _), (sq, sk, _) = fp8.fp8_inputs(to_f64(q), to_f64(k), to_f64(v))
+    assert np.array_equal(qz["sq"].cpu().numpy(), sq) and np.array_equal(qz["sk"].cpu().numpy(), sk)
+    q_dev = codes_to_f64(qz["q8"]) * np.repeat(sq, 128, axis=-1)[..., :Nq, None]
+    k_dev = codes_to_f64(qz["k8"]) * np.repeat(sk, 128, axis=-1)[..., :Nkv, None]
+    assert np.array_equal(q_dev, qd) and np.array_equal(k_dev, kd)
+
+
 def run_fp8(B, Hq, Hkv, Nq, Nkv, causal, seed, nrows=0):
     q, k, v = make_qkv(B, Hq, Hkv, Nq, Nkv, 128, seed)
     scale = 1.0 / math.sqrt(128)
