@@ -283,7 +283,7 @@ const char *attn_strerror(int code) {
 const char *attn_last_cuda_error(void) { return attn::t_last_error; }
 
 int attn_set_debug(int flags, long long wait_limit_ns) {
-  if (flags & ~(ATTN_DEBUG_DROP_V_COPY | ATTN_DEBUG_NO_CLUSTER)) return ATTN_ERR_ARG;
+  if (flags & ~(ATTN_DEBUG_DROP_V_COPY | ATTN_DEBUG_NO_CLUSTER | ATTN_DEBUG_HOST_CHUNKS)) return ATTN_ERR_ARG;
   if (wait_limit_ns < 0) return ATTN_ERR_ARG;
   attn::g_debug_flags.store(flags);
   attn::g_wait_limit_ns.store(wait_limit_ns == 0 ? (long long)attn::kWaitLimitNs : wait_limit_ns);

@@ -169,7 +169,10 @@ ATTN_API int attn_fwd_masked(const void *q, const void *k, const void *v, const 
  * memory: the caller may reuse every buffer at once.
  *
  * The work is cut by (b, kv head) group -- independent attention problems
- * whose rows are contiguous -- into up to four chunks; a chunk's inputs go up
+ * whose rows are contiguous -- into chunks of about 25 MiB of inputs (at most
+ * 8, at most one per group; measured best on GB300 for 100-200 MB problems,
+ * where more chunks lost to the copies of the two directions sharing the
+ * host link); a chunk's inputs go up
  * on a copy stream of the library's, its kernels run on a compute stream of
  * the library's (one per chunk) as soon as they have landed, and its outputs
  * come down on a second copy stream, so that the copies of one chunk overlap
@@ -332,13 +335,18 @@ ATTN_API int attn_fwd_status(attn_stream_t stream);
  *   ATTN_DEBUG_NO_CLUSTER, which runs head dims 384 ... 1024 on the
  *     per-slice Split-D kernel (each output slice recomputes the scores)
  *     instead of the cluster kernel, the path a device takes when it cannot
- *     hold one cluster; results agree within the parity tolerances.
+ *     hold one cluster; results agree within the parity tolerances;
+ *   ATTN_DEBUG_HOST_CHUNKS, which makes attn_fwd_host cut every problem into
+ *     one chunk per (b, kv head) group (up to its most, 8), whatever its size,
+ *     so that small problems take the chunked copy path; results stay
+ *     bit-identical to attn_fwd.
  * wait_limit_ns: bound on every device-side wait; 0 restores the default
  *   (2 s).
  * Returns ATTN_OK or ATTN_ERR_ARG.
  */
 #define ATTN_DEBUG_DROP_V_COPY 1
 #define ATTN_DEBUG_NO_CLUSTER 2
+#define ATTN_DEBUG_HOST_CHUNKS 4
 ATTN_API int attn_set_debug(int flags, long long wait_limit_ns);
 
 /* Static description of a return code. */

@@ -42,7 +42,7 @@ int main(int argc, char **argv) {
   CHECK(attn_fwd_splitkv(p, p, p, p, lp, 1, 2, 1, 8, 8, 64, 0.125f, 0, 65, NULL) == ATTN_ERR_ARG);
   CHECK(attn_fwd_splitkv_noalloc(p, p, p, p, lp, 1, 2, 1, 8, 8, 64, 0.125f, 0, 0, NULL) == ATTN_ERR_ARG);
   CHECK(attn_fwd_plan(1, 2, 1, 8, 8, 65, 0, &plan) == ATTN_ERR_ARG);
-  CHECK(attn_set_debug(4, 0) == ATTN_ERR_ARG);
+  CHECK(attn_set_debug(8, 0) == ATTN_ERR_ARG);
 
   /* an empty problem succeeds without touching a device */
   CHECK(attn_fwd(NULL, NULL, NULL, NULL, NULL, 0, 2, 1, 8, 8, 64, 0.125f, 0, NULL) == ATTN_OK);

@@ -116,7 +116,8 @@ def test_host_entry_argument_errors(lib):
 
 def test_set_debug_arguments(lib):
     lib.attn_set_debug.argtypes = [ctypes.c_int, ctypes.c_longlong]
-    assert lib.attn_set_debug(4, 0) == -1
+    assert lib.attn_set_debug(8, 0) == -1
+    assert lib.attn_set_debug(2 | 4, 0) == 0
     assert lib.attn_set_debug(2, 0) == 0
     assert lib.attn_set_debug(0, -5) == -1
     assert lib.attn_set_debug(1, 1000000) == 0

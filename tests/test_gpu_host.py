@@ -1,20 +1,25 @@
 """attn_fwd_host (host buffers, copies overlapped with the kernels by chunks of
 (b, kv head) groups) against attn_fwd on the device: bit-identical O and LSE,
-and the oracle's tolerances on one case."""
+and the oracle's tolerances on one case.  These problems are small enough to
+go in one chunk by size; ATTN_DEBUG_HOST_CHUNKS makes the same calls take one
+chunk per group, so both forms are checked."""
 import pytest
 import torch
 
-from exact_attention_attn_gb300 import attn_fwd, attn_fwd_host, attn_fwd_status
+from exact_attention_attn_gb300 import attn_fwd, attn_fwd_host, attn_fwd_status, attn_set_debug
 from exact_attention_attn_gb300.workloads import make_qkv
 
 from parity_util import compare
 
 pytestmark = pytest.mark.gpu
 
+ATTN_DEBUG_HOST_CHUNKS = 4
+
 CASES = [
     # B, Hq, Hkv, Nq, Nkv, D, causal
-    (2, 8, 2, 300, 300, 128, True),     # GQA, four chunks of two groups
-    (1, 3, 3, 129, 200, 64, False),     # three chunks; LSE rows of 129 floats per head
+    (2, 8, 2, 300, 300, 128, True),     # GQA; chunked: four chunks of one group
+    (1, 3, 3, 129, 200, 64, False),     # chunked: three chunks; LSE rows of 129 floats per head
+    (2, 10, 10, 200, 200, 64, True),    # chunked: twenty groups in eight chunks of two or three
     (2, 4, 4, 1000, 5000, 128, False),  # few row tiles: the key split count of the whole problem
     (1, 2, 1, 100, 0, 128, False),      # no keys
     (1, 4, 4, 256, 300, 512, True),     # Split-D kernel
@@ -30,13 +35,18 @@ def _status_clean():
 
 @pytest.mark.parametrize("case", CASES, ids=[str(c) for c in CASES])
 @pytest.mark.parametrize("pinned", [True, False])
-def test_host_matches_device(case, pinned):
+@pytest.mark.parametrize("chunked", [False, True])
+def test_host_matches_device(case, pinned, chunked):
     B, Hq, Hkv, Nq, Nkv, D, causal = case
     q, k, v = make_qkv(B, Hq, Hkv, Nq, Nkv, D, seed=Nq + Nkv + D)
     scale = D ** -0.5
     if pinned:
         q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    o_h, l_h = attn_fwd_host(q, k, v, scale=scale, causal=causal)
+    attn_set_debug(ATTN_DEBUG_HOST_CHUNKS if chunked else 0, 0)
+    try:
+        o_h, l_h = attn_fwd_host(q, k, v, scale=scale, causal=causal)
+    finally:
+        attn_set_debug(0, 0)
     o_d, l_d = attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=causal)
     torch.cuda.synchronize()
     assert o_h.device.type == "cpu" and l_h.device.type == "cpu"
