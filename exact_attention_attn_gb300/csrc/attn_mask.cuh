@@ -4,10 +4,10 @@
 // the key.  In the kernels' base-2 units the score of key j becomes
 //     y_j = s_j * (scale * log2 e) + mask_j * log2 e.
 //
-// Two ways to bring a row's 128 values of one key block on chip:
-//   - mask_load128: straight into 64 registers (bf16 pairs), for a kernel
-//     with registers to spare; issued before the thread waits for its scores
-//     so that the load latency hides behind that wait;
+// Ways to bring a row's values of one key block on chip:
+//   - mask_load<NV>: NV values straight into NV / 2 registers (bf16 pairs),
+//     issued before the thread waits for its scores so that the load latency
+//     hides behind that wait;
 //   - mask_stage128: cp.async into shared memory, 16 chunks of 8 values laid
 //     out chunk-major ([16][nrows][16 bytes]) so that a warp's 16-byte reads
 //     of one chunk are contiguous; for kernels whose registers are taken.
@@ -34,13 +34,26 @@ __device__ __forceinline__ const __nv_bfloat16 *mask_row(const Problem &p, int b
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// mk[i] = values of keys kbase + 2i, kbase + 2i + 1 (zero where the key is
-// >= nkv or row is null).  Whole 16-byte vectors are loaded where they lie
-// below nkv, the one ragged vector value by value.
-__device__ __forceinline__ void mask_load128(uint32_t (&mk)[64], const __nv_bfloat16 *row, int kbase, int nkv) {
-  const int n = row ? nkv - kbase : 0;  // valid values in this block
+// mk[i] = values of keys kbase + 2i, kbase + 2i + 1, i < NV / 2 (zero where
+// the key is >= nkv or row is null).  Whole 16-byte vectors are loaded where
+// they lie below nkv, the one ragged vector value by value.
+template <int NV>
+__device__ __forceinline__ void mask_load(uint32_t (&mk)[NV / 2], const __nv_bfloat16 *row, int kbase, int nkv) {
+  const int n = row ? nkv - kbase : 0;  // valid values from kbase on
+  if (n >= NV) {  // every value below nkv: plain vector loads
+    const uint4 *src = reinterpret_cast<const uint4 *>(row + kbase);
 #pragma unroll
-  for (int v = 0; v < 16; ++v) {
+    for (int v = 0; v < NV / 8; ++v) {
+      const uint4 w = __ldg(src + v);
+      mk[4 * v + 0] = w.x;
+      mk[4 * v + 1] = w.y;
+      mk[4 * v + 2] = w.z;
+      mk[4 * v + 3] = w.w;
+    }
+    return;
+  }
+#pragma unroll
+  for (int v = 0; v < NV / 8; ++v) {
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
     if (8 * v + 8 <= n) {
       w = __ldg(reinterpret_cast<const uint4 *>(row + kbase + 8 * v));

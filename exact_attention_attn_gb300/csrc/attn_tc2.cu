@@ -140,6 +140,33 @@ __device__ __forceinline__ void raise_abort(Bars2 *bars, int *status) {
   *reinterpret_cast<volatile int *>(&bars->abort) = 1;
 }
 
+// One quarter (32 keys) of a masked block for one row: y = s * scale + mask
+// (natural-log units) on f32x2 pairs into y2[0..16), the block max in two
+// chains.  CUT: keys at or past vis_end give -inf (blocks where some row of
+// the warp has such keys).
+template <bool CUT>
+__device__ __forceinline__ void mask_quarter(const uint32_t (&cur)[32], const uint32_t *mk16, uint64_t *y2,
+                                             uint64_t sc2, int key0, int vis_end, float &mx0, float &mx1) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t w = mk16[i];
+    uint64_t v = f2_fma(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), sc2,
+                        f2_pack(bf16_lo(w), bf16_hi(w)));
+    float y0, y1;
+    f2_unpack(v, y0, y1);
+    if (CUT) {
+      if (key0 + 2 * i >= vis_end) y0 = -INFINITY;
+      if (key0 + 2 * i + 1 >= vis_end) y1 = -INFINITY;
+      v = f2_pack(y0, y1);
+    }
+    y2[i] = v;
+    if (i & 1)
+      mx1 = max3f(mx1, y0, y1);
+    else
+      mx0 = max3f(mx0, y0, y1);
+  }
+}
+
 // MODE 0: the scale is positive (scores and their maxima keep their order);
 // MODE 1: the scale is zero or negative (block minima of the raw scores);
 // MODE 2: an additive mask, either sign (block maxima of the masked, scaled
@@ -417,17 +444,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool full = kbase + BN <= vis_end;  // no masked key in this block for this row
       // the mask values of this row and block, on their way while S_t,j is computed
       uint32_t mk[MASK ? 64 : 1];
-      if constexpr (MASK) mask_load128(mk, mrow, kbase, p.Nkv);
+      if constexpr (MASK) mask_load<128>(mk, mrow, kbase, p.Nkv);
       if (tr) ATTN_TRACE_EV(4 * t + 0, j);
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abortf, limit))) { ok = false; break; }
       if (tr) ATTN_TRACE_EV(4 * t + 1, j);
       tc_fence_after();
       float mblk;
-      float y[MASK ? BN : 1];
+      uint64_t y2[MASK ? BN / 2 : 1];
       if constexpr (MASK) {
-        // y = s * sl2 + mask * log2 e (-inf past vis_end), kept for P; block
-        // max of y.  The scores are read a quarter at a time, so that each
-        // quarter's mask values are dead once used
+        // y = s * scale + mask (natural-log units, kept for P) a quarter at a
+        // time, so that each quarter's mask values are dead once used; the
+        // block max of y times log2 e is the block max of the log2-unit scores
+        // (rounding is monotone)
+        const bool cut = !__all_sync(0xffffffffu, full);
+        const uint64_t sc2 = f2_pack(p.scale, p.scale);
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -435,20 +465,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(tS + 32 * h, cur);
           tmem_wait_ld();
           reg_fence32(cur);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = 32 * h + 2 * i;
-            const uint32_t w = mk[16 * h + i];
-            y[c] = (kbase + c >= vis_end) ? -INFINITY : fmaf(__uint_as_float(cur[2 * i]), sl2, kLog2e * bf16_lo(w));
-            y[c + 1] =
-                (kbase + c + 1 >= vis_end) ? -INFINITY : fmaf(__uint_as_float(cur[2 * i + 1]), sl2, kLog2e * bf16_hi(w));
-            if (i & 1)
-              mx1 = max3f(mx1, y[c], y[c + 1]);
-            else
-              mx0 = max3f(mx0, y[c], y[c + 1]);
-          }
+          if (cut)
+            mask_quarter<true>(cur, mk + 16 * h, y2 + 16 * h, sc2, kbase + 32 * h, vis_end, mx0, mx1);
+          else
+            mask_quarter<false>(cur, mk + 16 * h, y2 + 16 * h, sc2, kbase + 32 * h, vis_end, mx0, mx1);
         }
-        mblk = fmaxf(mx0, mx1);
+        mblk = fmaxf(mx0, mx1) * kLog2e;
       } else {
       uint32_t sr[4][32];
 #pragma unroll
@@ -512,21 +534,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the branch must be warp-uniform: both sides end in the warp-collective
       // tcgen05.st, which every lane of the warp has to execute together
       if constexpr (MASK) {
-        // P = 2^(y - mu), a quarter at a time into columns [16h, 16h+16)
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // P = 2^(y log2 e - mu), a quarter at a time into columns [16h, 16h+16)
+        const uint64_t l2e2 = f2_pack(kLog2e, kLog2e), nmu2 = f2_pack(-mu, -mu);
+        uint64_t acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int c = 32 * h + 2 * i;
-            const float p0 = ex2_approx(y[c] - mu), p1 = ex2_approx(y[c + 1] - mu);
-            ls[i & 3] += p0 + p1;
+            float a0, a1;
+            f2_unpack(f2_fma(y2[16 * h + i], l2e2, nmu2), a0, a1);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            if (i & 1)
+              acc1 = f2_add(acc1, f2_pack(p0, p1));
+            else
+              acc0 = f2_add(acc0, f2_pack(p0, p1));
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tS + h * 16, pk);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        float s0, s1, s2, s3;
+        f2_unpack(acc0, s0, s1);
+        f2_unpack(acc1, s2, s3);
+        l += (s0 + s1) + (s2 + s3);
       } else if (pos && __all_sync(0xffffffffu, full)) {
         // every key visible and scale > 0: y = s*sl2 - mu on f32x2 pairs,
         // exp2 on the MUFU (pairs selected by kPolyPairs on the FMA pipe)
