@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       const int kbase = j * BT;
       // the scores a quarter (32 keys) at a time, the next quarter's load in
       // flight while this one is turned into P
-      uint32_t pb[BT / 2];  // P as bf16 pairs
+      float pf[BT];  // P in fp32 (dS = P (dP - Delta) is rounded once, to bf16)
       uint32_t qb[2][32];
       tmem_ld32(tR, qb[0]);
       tmem_wait_ld();
@@ -676,9 +676,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const int c = kbase + 32 * h + i;
-          const float p0 = (c < vis_end) ? ex2_approx(fmaf(__uint_as_float(cur[i]), sl2, -lse2)) : 0.f;
-          const float p1 = (c + 1 < vis_end) ? ex2_approx(fmaf(__uint_as_float(cur[i + 1]), sl2, -lse2)) : 0.f;
-          pb[16 * h + (i >> 1)] = pack_bf16x2(p0, p1);
+          pf[32 * h + i] = (c < vis_end) ? ex2_approx(fmaf(__uint_as_float(cur[i]), sl2, -lse2)) : 0.f;
+          pf[32 * h + i + 1] = (c + 1 < vis_end) ? ex2_approx(fmaf(__uint_as_float(cur[i + 1]), sl2, -lse2)) : 0.f;
         }
         if (h < 3) {
           tmem_wait_ld();
@@ -701,9 +700,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const uint32_t w = pb[16 * h + (i >> 1)];
-          pk[i >> 1] = pack_bf16x2(__uint_as_float(w << 16) * (__uint_as_float(cur[i]) - delta),
-                                   __uint_as_float(w & 0xffff0000u) * (__uint_as_float(cur[i + 1]) - delta));
+          pk[i >> 1] = pack_bf16x2(pf[32 * h + i] * (__uint_as_float(cur[i]) - delta),
+                                   pf[32 * h + i + 1] * (__uint_as_float(cur[i + 1]) - delta));
         }
         tmem_st16(tR + 16 * h, pk);
         if (h < 3) {

@@ -315,3 +315,39 @@ def attention_backward(q, k, v, do, scale, causal, mask=None):
             dk[b, kv] += gk
             dv[b, kv] += gv
     return dq, dk, dv
+
+
+def attention_backward_sampled(q, k, v, do, scale, causal, rows, keys, block: int = 1024):
+    """Chosen entries of one head's gradients, for heads too long to form
+    N x N matrices: dq at query rows `rows` and the head's contribution to
+    dk, dv at keys `keys`, by the formulas of attention_backward_head (the
+    chain rule through the row softmax).  P is formed `block` query rows at
+    a time (probs_head on those rows), so memory stays at block x Nkv; each
+    row block adds its terms of dV[keys] = sum_i P_i,keys dO_i and
+    dK[keys] = scale sum_i dS_i,keys Q_i, with Delta_i = dO_i . O_i and
+    O_i = sum_j P_ij V_j of its own rows.
+    Returns (dq [len(rows), D], dk [len(keys), D], dv [len(keys), Dv])."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = np.asarray(keys, dtype=np.int64)
+    Nq = q.shape[0]
+    dq = np.zeros((len(rows), q.shape[1]))
+    dk = np.zeros((len(keys), k.shape[1]))
+    dv = np.zeros((len(keys), v.shape[1]))
+    for r0 in range(0, Nq, block):
+        idx = np.arange(r0, min(Nq, r0 + block))
+        P = probs_head(q, k, scale, causal, idx)          # [b, Nkv]
+        delta = (do[idx] * (P @ v)).sum(axis=1)            # Delta_i = dO_i . O_i
+        Pk = P[:, keys]
+        dSk = Pk * (do[idx] @ v[keys].T - delta[:, None])  # dS at the chosen keys
+        dv += Pk.T @ do[idx]
+        dk += scale * (dSk.T @ q[idx])
+        sel = np.nonzero((rows >= idx[0]) & (rows <= idx[-1]))[0]
+        for s in sel:                                       # dQ rows of this block
+            i = rows[s] - r0
+            dS_row = P[i] * (do[rows[s]] @ v.T - delta[i])
+            dq[s] = scale * (dS_row @ k)
+    return dq, dk, dv

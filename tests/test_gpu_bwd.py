@@ -119,3 +119,65 @@ def test_backward_rejects_unsupported_head_dim():
     o, lse = attn_fwd(q, k, v)
     with pytest.raises(AttnError):
         attn_bwd(q, k, v, o, lse, o.clone())
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def emulated_sampled(q, k, v, do, scale, rows, keys, block=1024):
+    """The sampled causal gradients of one head with exactly the kernels'
+    documented roundings applied to the float64 quantities: Delta from the
+    bf16 O, dS = P (dP - Delta) rounded to bf16 before both products, P
+    rounded to bf16 before dV's, dq, dk, dv rounded to bf16 once."""
+    N = q.shape[0]
+    dq = np.zeros((len(rows), q.shape[1]))
+    dk = np.zeros((len(keys), k.shape[1]))
+    dv = np.zeros((len(keys), v.shape[1]))
+    for r0 in range(0, N, block):
+        idx = np.arange(r0, min(N, r0 + block))
+        P = oracle.probs_head(q, k, scale, True, idx)
+        delta = (do[idx] * _bf16(P @ v)).sum(axis=1)
+        dSk = _bf16(P[:, keys] * (do[idx] @ v[keys].T - delta[:, None]))
+        dv += _bf16(P[:, keys]).T @ do[idx]
+        dk += scale * (dSk.T @ q[idx])
+        for s_, r in enumerate(rows):
+            if idx[0] <= r <= idx[-1]:
+                i = r - r0
+                dq[s_] = scale * (_bf16(P[i] * (do[r] @ v.T - delta[i])) @ k)
+    return dq, dk, dv
+
+
+def test_backward_bench_shape_sampled():
+    # the backward at the size bench.py --path bwd times (GQA causal B2 Hq32
+    # Hkv8 N8192 D128, the same launches), checked on entries the oracle
+    # computes without N x N matrices: dq at sampled rows of the four query
+    # heads of one (b, kv head) group, dk and dv at sampled keys of that kv
+    # head (the group's sum).  Rows of 8192 keys sum 8192 rounded dS terms
+    # whose row sums cancel, so the small shapes' fixed bound does not carry
+    # over: here each error may be at most twice that of an emulation of the
+    # kernels' roundings (emulated_sampled) on the same entries.
+    B, Hq, Hkv, N, D = 2, 32, 8, 8192, 128
+    (q, k, v, do, scale), (gq, gk, gv) = grads(B, Hq, Hkv, N, N, D, True, seed=81)
+    b, kvh, g = 1, 5, Hq // Hkv
+    rng = np.random.default_rng(82)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 4095, N - 1], rng.integers(0, N, 10)]))
+    keys = np.unique(np.concatenate([[0, 1, 127, 128, 4096, N - 2, N - 1], rng.integers(0, N, 9)]))
+    kk, vv = to_f64(k[b, kvh]), to_f64(v[b, kvh])
+    ref_k, emu_k = np.zeros((2, len(keys), D)), np.zeros((2, len(keys), D))
+
+    def within(name, got, ref, emu):
+        e_got, e_emu = np.abs(got - ref), np.abs(_bf16(emu) - ref)
+        tiny = 1e-6 * np.abs(ref).max()
+        assert e_got.max() <= 2 * e_emu.max() + tiny, (name, e_got.max(), e_emu.max())
+        assert e_got.mean() <= 2 * e_emu.mean() + tiny, (name, e_got.mean(), e_emu.mean())
+
+    for h in range(kvh * g, kvh * g + g):
+        qh, doh = to_f64(q[b, h]), to_f64(do[b, h])
+        dq_ref, dk_h, dv_h = oracle.attention_backward_sampled(qh, kk, vv, doh, scale, True, rows, keys)
+        dq_emu, dke, dve = emulated_sampled(qh, kk, vv, doh, scale, rows, keys)
+        ref_k += (dk_h, dv_h)
+        emu_k += (dke, dve)
+        within(f"dq head {h}", to_f64(gq[b, h])[rows], dq_ref, dq_emu)
+    within("dk", to_f64(gk[b, kvh])[keys], ref_k[0], emu_k[0])
+    within("dv", to_f64(gv[b, kvh])[keys], ref_k[1], emu_k[1])

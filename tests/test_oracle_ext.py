@@ -442,3 +442,20 @@ def test_bwd_pins_catch_planted_mistake(kind):
             except Exception:
                 errs.append(math.inf)
     assert max(errs) > 1e-5, f"backward mutant {kind} passed every pin"
+
+
+@pytest.mark.parametrize("shape", [(37, 37), (50, 23), (23, 61)])
+def test_backward_sampled_matches_full_backward(shape):
+    # the blocked, sampled gradients equal the entries of the full backward
+    # (itself pinned by torch autograd, finite differences and closed forms),
+    # with blocks smaller than the rows, a ragged last block, causal or not
+    Nq, Nkv = shape
+    q, k, v, do = rnd((Nq, 8), 700), rnd((Nkv, 8), 701), rnd((Nkv, 8), 702), rnd((Nq, 8), 703)
+    rows = np.array([0, 5, Nq // 2, Nq - 1])
+    keys = np.array([0, 3, Nkv // 2, Nkv - 1])
+    for causal in (False, True):
+        full = oracle.attention_backward_head(q, k, v, do, 0.35, causal)
+        dq, dk, dv = oracle.attention_backward_sampled(q, k, v, do, 0.35, causal, rows, keys, block=16)
+        assert np.allclose(dq, full[0][rows], rtol=0, atol=1e-12)
+        assert np.allclose(dk, full[1][keys], rtol=0, atol=1e-12)
+        assert np.allclose(dv, full[2][keys], rtol=0, atol=1e-12)
