@@ -154,3 +154,9 @@ def test_zero_mask_matches_unmasked(D):
 def test_mask_large_workload_sampled():
     # the causal GQA N2048 D128 shape with one mask shared by every head
     run_case(2, 8, 2, 2048, 2048, 128, True, (1, 1, 2048, 2048), seed=31, nrows=128)
+
+
+def test_mask_bench_shape_sampled():
+    # the size bench.py --path mask times: GQA causal B2 Hq32 Hkv8 N8192 D128,
+    # one [Nq, Nkv] mask shared by every head, 64 sampled rows per head
+    run_case(2, 32, 8, 8192, 8192, 128, True, (1, 1, 8192, 8192), seed=41, nrows=64)
