@@ -84,6 +84,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd_plan.restype = ci
         lib.attn_version.argtypes = []
         lib.attn_version.restype = ci
+        lib.attn_shutdown.argtypes = []
+        lib.attn_shutdown.restype = ci
         _lib = lib
         return lib
 
@@ -98,6 +100,13 @@ def _last_cuda_error() -> str:
 
 def attn_version() -> int:
     return int(load_library().attn_version())
+
+
+def attn_shutdown() -> None:
+    """Give back the device memory of the library's pools: see attn_shutdown in include/attn.h."""
+    rc = load_library().attn_shutdown()
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_shutdown")
 
 
 def _stream_handle(stream) -> int:

@@ -265,6 +265,30 @@ extern "C" {
 
 int attn_version(void) { return 100; /* 0.1.0 */ }
 
+int attn_shutdown(void) {
+  int cur = 0;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return attn::record(e);
+  cudaError_t first = cudaSuccess;
+  for (int dev = 0; dev < attn::kMaxDevices; ++dev) {
+    cudaMemPool_t pool = nullptr;
+    {
+      std::lock_guard<std::mutex> lock(attn::g_dev_mu);
+      pool = attn::g_dev[dev].ws_pool;
+    }
+    if (!pool) continue;
+    // every stream-ordered free has completed once the device is idle
+    if ((e = cudaSetDevice(dev)) == cudaSuccess && (e = cudaDeviceSynchronize()) == cudaSuccess)
+      e = cudaMemPoolTrimTo(pool, 0);
+    if (first == cudaSuccess) first = e;
+  }
+  e = attn::release_host_copy_memory();
+  if (first == cudaSuccess) first = e;
+  e = cudaSetDevice(cur);
+  if (first == cudaSuccess) first = e;
+  return first == cudaSuccess ? ATTN_OK : attn::record(first);
+}
+
 const char *attn_strerror(int code) {
   switch (code) {
     case ATTN_OK: return "ok";

@@ -50,6 +50,20 @@ CopyStreams g_copy[kMaxDev];
 std::mutex g_copy_mu[kMaxDev];
 
 }  // namespace
+
+cudaError_t release_host_copy_memory() {
+  cudaError_t first = cudaSuccess;
+  for (int dev = 0; dev < kMaxDev; ++dev) {
+    std::lock_guard<std::mutex> lock(g_copy_mu[dev]);
+    if (!g_copy[dev].pool) continue;
+    cudaError_t e = cudaSetDevice(dev);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemPoolTrimTo(g_copy[dev].pool, 0);
+    if (first == cudaSuccess) first = e;
+  }
+  return first;
+}
+
 }  // namespace attn
 
 extern "C" int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,

@@ -99,6 +99,11 @@ cudaError_t launch_combine(const Problem &p, cudaStream_t stream);
 // Free with cudaFreeAsync on the same stream.
 cudaError_t scratch_alloc(void **ptr, size_t bytes, cudaStream_t st);
 
+// Waits for every device whose host-copy pool (attn_fwd_host) holds memory
+// and returns that pool's unused memory to the driver; leaves the current
+// device changed (the caller restores it).
+cudaError_t release_host_copy_memory();
+
 // Bound on device-side waits and debug flags currently set by attn_set_debug.
 uint64_t wait_limit_ns();
 int debug_flags();

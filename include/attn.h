@@ -381,6 +381,23 @@ ATTN_API int attn_fwd_plan(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int c
 /* Library version as major * 10000 + minor * 100 + patch. */
 ATTN_API int attn_version(void);
 
+/*
+ * attn_shutdown -- give back the device memory the library's pools hold.
+ *
+ * The split-KV workspace (attn_fwd, attn_fwd_splitkv, attn_fwd_masked,
+ * attn_bwd's per-row vectors) and the device copies of attn_fwd_host come
+ * from memory pools of the library's that keep their memory between calls.
+ * This call waits until every device the library has used for them is idle
+ * (cudaDeviceSynchronize on each, so also for work that is not the
+ * library's), then trims each pool to nothing.  The library stays usable:
+ * later calls grow the pools again.  The fixed 16 MiB scratch of
+ * attn_fwd_splitkv_noalloc is part of the loaded module and stays.
+ * Call it when no other thread is calling the library.
+ * Returns ATTN_OK, or ATTN_ERR_LAUNCH with the first CUDA error (see
+ * attn_last_cuda_error); the current device is restored.
+ */
+ATTN_API int attn_shutdown(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,3 +68,25 @@ def test_host_outputs_in_place():
     o, l = attn_fwd_host(q, k, v, causal=False, out=out, lse=lse)
     assert o.data_ptr() == out.data_ptr() and l.data_ptr() == lse.data_ptr()
     assert not torch.isnan(out.float()).any() and not torch.isnan(lse).any()
+
+
+def test_shutdown_gives_back_pools_and_library_stays_usable():
+    # a split-KV call (few row tiles, many keys) and a host-buffer call fill
+    # the library's two pools; attn_shutdown trims them, and the same calls
+    # afterwards give the same bits
+    from exact_attention_attn_gb300 import attn_fwd_plan, attn_shutdown
+    q, k, v = make_qkv(1, 2, 2, 64, 16384, 128, seed=21)
+    assert attn_fwd_plan(1, 2, 2, 64, 16384, 128, False)["kv_splits"] > 1
+    qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o1, l1 = attn_fwd(q.cuda(), k.cuda(), v.cuda())
+    oh1, lh1 = attn_fwd_host(qp, kp, vp)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    attn_shutdown()
+    assert torch.cuda.mem_get_info()[0] >= free_before
+    o2, l2 = attn_fwd(q.cuda(), k.cuda(), v.cuda())
+    oh2, lh2 = attn_fwd_host(qp, kp, vp)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(oh1, oh2) and torch.equal(lh1, lh2)
+    assert torch.equal(oh1, o1.cpu())
