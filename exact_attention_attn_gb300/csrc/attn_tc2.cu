@@ -804,7 +804,9 @@ cudaError_t launch_tc2_d(const Problem &p, int device, uint64_t wait_limit_ns, c
   memset(&prm, 0, sizeof(prm));
   prm.p = p;
   prm.npairs = ((p.Nq + BM - 1) / BM + 1) / 2;
-  prm.head_chunk = head_chunk(p, prm.npairs, device);
+  // a mask shared by every head is read best with all heads in step (the
+  // plain heaviest-first order): every head then reads each mask row at once
+  prm.head_chunk = (MODE == 2 && p.mask_sh == 0) ? p.B * p.Hq : head_chunk(p, prm.npairs, device);
   prm.kst = kst;
   prm.vst = vst;
   prm.off_k = qb;
