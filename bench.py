@@ -341,7 +341,9 @@ def run_reference(args, w):
         return 0
     q, k, v = make_workload_inputs(w)
     extra = path_host_inputs(args.path, w)
-    per_step_budget = 5.0
+    # about 100 s of oracle work for the whole run (5 s a step at 20 steps),
+    # at least half a second and one head a step
+    per_step_budget = min(5.0, max(0.5, 100.0 / max(args.steps, 1)))
     for _ in range(args.warmup):
         time_oracle(w, q, k, v, budget_s=0.0, max_heads=1, path=args.path, extra=extra)
     vals, heads_total, secs, nrows = [], 0, 0.0, w.Nq
@@ -353,7 +355,7 @@ def run_reference(args, w):
     value = statistics.mean(vals)
     cores = blas_threads() or cpu_cores()
     sample = (oracle_sample_text(w, heads_total, secs, nrows, cores, args.path) +
-              f"; {args.steps} steps, each stopping after {per_step_budget:.0f} s")
+              f"; {args.steps} steps, each stopping after {per_step_budget:.1f} s")
     flops_per_head = (2.5 if args.path == "bwd" else 1.0) * w.flops() / (w.B * w.Hq)
     line = {
         "impl": "reference", "metric": PATHS[args.path][0] or METRIC, "value": value, "unit": "TFLOPS",
