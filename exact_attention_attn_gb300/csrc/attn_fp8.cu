@@ -23,10 +23,13 @@
 //     (two 128-row query tiles per CTA sharing every K and V block), with
 //     S = Q8 K8^T on kind::f8f6f4; the softmax works on s * (scale * sq *
 //     sk * log2 e) (sq, sk the tile's and the block's scales); P is written
-//     as 2^(y - m + 8) rounded to e4m3 (the factor 2^8 puts P in the upper
-//     binades of e4m3, and the lazy rescale threshold of 0.5 in log2 units
-//     keeps it below 2^8.5 < 448); O = sv * (P8 V8) / l with l the fp32 sum
-//     of the same 2^(y - m + 8).
+//     as 2^(y - m + 2) rounded to e4m3 (the factor 2^2 and the lazy rescale
+//     threshold of 6.5 in log2 units keep it below 2^8.5 < 448; e4m3 rounds
+//     relative to each value, so the factor moves only the few p below
+//     2^-8 into subnormals, and the large threshold spares the O rescales
+//     that a threshold of 0.5 with a factor 2^8 cost: 1450 -> 1719 TFLOP/s
+//     on GQA causal N8192); O = sv * (P8 V8) / l with l the fp32 sum of the
+//     same 2^(y - m + 2).
 //
 // Since (Q H)(K H)^T = Q K^T, the result approximates exact attention on
 // the original inputs; it equals exact attention on the dequantised inputs
@@ -52,8 +55,8 @@ constexpr int TILE = 128 * 128;         // one 128-row x 128-byte e4m3 tile
 constexpr float kInvSqrtD = 0.08838834764831845f;  // 1/sqrt(128), rounded to float32
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float TAU = 0.5f;             // lazy rescale threshold, log2 units
-constexpr float P_SHIFT = 8.f;          // P is stored as 2^8 p
+constexpr float TAU = 6.5f;             // lazy rescale threshold, log2 units
+constexpr float P_SHIFT = 2.f;          // P is stored as 2^2 p
 constexpr int THREADS = 352;
 constexpr int WARP_LOAD_K = 8, WARP_LOAD_V = 10, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
@@ -577,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         l *= alpha;
         m_use = m_new;
       }
-      // 2^8 p = 2^(s c - m + 8); quarter h of the keys lands as e4m3 in
+      // 2^2 p = 2^(s c - m + 2); quarter h of the keys lands as e4m3 in
       // columns [8h, 8h + 8), all inside the first quarter, already read
       const float bias = P_SHIFT - ((m_use == -INFINITY) ? 0.f : m_use);
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -646,7 +649,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (!ok) raise_abort(bars, prm.status);
 
-    // ---- epilogue: O = sv * acc / l (l holds 2^8 times the sum of p)
+    // ---- epilogue: O = sv * acc / l (l holds 2^2 times the sum of p)
     if (ok && nb > 0) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], 0, abortf, limit))) {
         raise_abort(bars, prm.status);

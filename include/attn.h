@@ -294,8 +294,8 @@ ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o
  * attn_fwd_fp8 computes O (bf16 [B, Hq, Nq, 128]) and LSE (fp32 [B, Hq, Nq])
  * from them: S = sq sk (q8 k8^T) on the FP8 tensor cores (the rotation
  * cancels: (qH)(kH)^T = q k^T), the online softmax of attn_fwd with a lazy
- * rescale threshold of 0.5 (log2 units), P rounded to e4m3 as 2^8 p, and
- * O = sv (P8 v8) / (2^8 l) with l the fp32 sum of p.  The result approximates
+ * rescale threshold of 6.5 (log2 units), P rounded to e4m3 as 2^2 p, and
+ * O = sv (P8 v8) / (2^2 l) with l the fp32 sum of p.  The result approximates
  * attn_fwd's; it equals exact attention on the dequantised inputs up to the
  * e4m3 rounding of P.
  *

@@ -35,7 +35,7 @@ notes):
    (k = 0 for an all-zero block); codes are e4m3(x / 2^k).
 4. The reference for the kernel is exact attention (the float64 oracle) on
    the dequantised inputs 2^k e4m3(x / 2^k).  The kernel also rounds P to
-   e4m3 (times 2^8, divided back out); that rounding is an approximation
+   e4m3 (times a power of two, divided back out); that rounding is an approximation
    the tolerance accounts for, not part of this reference.
 """
 from __future__ import annotations

@@ -4,7 +4,7 @@ FP8 oracle (oracle/fp8.py), through the C ABI.
 Quantisation decides integer codes, so both sides take it in float32 in the
 same butterfly order and the codes and scales must match exactly.  The
 attention output is compared with exact (float64) attention on the
-dequantised inputs; the kernel also rounds P to e4m3 (as 2^8 p), which the
+dequantised inputs; the kernel also rounds P to e4m3 (as 2^2 p), which the
 tolerance covers: max|dO| <= 0.1, mean|dO| <= 1e-2, max|dLSE| <= 1e-3.
 Derivation: e4m3 keeps 3 mantissa bits, so each probability carries a
 relative error of up to 2^-4; an emulation of exactly that rounding on the
